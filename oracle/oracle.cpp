@@ -1,0 +1,362 @@
+// CPU oracle for the embedding backward pass with a fused row optimizer.
+//
+// TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the
+// cpu_baseline / reference leg of bench.py may load this library. The product
+// path (the CUDA library under sparse_embedding_bag_gb300/) never calls it and
+// shares no code, header, table or helper with it.
+//
+// Plain, slow, single-threaded C++ that follows the definition of the
+// operation step by step:
+//   1. linearise every lookup i of bag (t, b) to hash_size_cumsum[t] + indices[i]
+//      ("fbgemm_gpu/codegen/embedding_backward_split_template.cu",
+//       kernels *_kernel_cta_per_row_1 / *_kernel_warp_per_row_1: the linear
+//       index and the hash_size_cumsum subtraction; "tt_embeddings_cuda.cu",
+//       compute_rowidx_kernel: the CSR bag expansion, table-major);
+//   2. sort the (linear index, lookup id) pairs with std::sort;
+//   3. run-length encode the sorted keys, exclusive scan of run lengths, and
+//      the set of runs at least max_segment_length_per_warp long
+//      ("embedding_backward_split_template.cu", *_find_long_segments);
+//   4. accumulate, in double, for every unique row the sum of the scaled
+//      gradient rows of its lookups: scale = per_sample_weight (if weighted)
+//      times 1/L (if mean pooling) ("embedding_backward_split_template.cu",
+//      grad_mean_kernel and the weighted fma in the per-row kernels);
+//   5. apply the optimizer once per unique row, in double:
+//        SGD:              w <- w - lr * G
+//          ("tt_embeddings_cuda.cu", update_tt_cores_sgd_kernel,
+//           cache_backward_sgd_kernel)
+//        row-wise Adagrad: m <- m + sum_d(G_d^2) / D ; w <- w - lr * G / (sqrt(m) + eps)
+//          ("tt_embeddings_cuda.cu", cache_backward_rowwise_adagrad_approx_kernel:
+//           mean of squares over D, state updated before use, eps outside the
+//           square root), applied to the de-duplicated row gradient;
+//   6. round w to its storage type (round to nearest, ties to even) and m to fp32.
+//
+// Every function here is pinned by tests/test_oracle_*.py against brute force
+// (a dense one-hot matrix product), closed forms and invariants.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+enum { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+enum { OK = 0, ERR_INVALID_ARG = 1, ERR_UNSUPPORTED = 2, ERR_INDEX_OUT_OF_RANGE = 3 };
+
+// ---- storage-type conversions, written from the IEEE 754 binary16 and the
+// ---- bfloat16 (binary32 with the low 16 mantissa bits dropped) formats.
+
+double half_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1F;
+  const int m = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = std::ldexp(static_cast<double>(m), -24);  // subnormal: m * 2^-24
+  } else if (e == 31) {
+    v = m ? NAN : INFINITY;
+  } else {
+    v = std::ldexp(static_cast<double>(1024 + m), e - 25);  // (1 + m/1024) * 2^(e-15)
+  }
+  return sign ? -v : v;
+}
+
+// Direct double -> binary16 with round-to-nearest-even (no intermediate fp32,
+// so there is no double rounding).
+uint16_t double_to_half(double x) {
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  if (std::isnan(x)) return sign | 0x7E00;
+  const double a = std::fabs(x);
+  if (a == 0.0) return sign;
+  if (a < std::ldexp(1.0, -14)) {
+    // subnormal grid: multiples of 2^-24. rint rounds half to even.
+    const double q = std::rint(std::ldexp(a, 24));
+    return sign | static_cast<uint16_t>(q);  // q == 1024 encodes the smallest normal
+  }
+  int e2;
+  std::frexp(a, &e2);  // a = f * 2^e2, f in [0.5, 1)
+  int E = e2 - 1;      // a in [2^E, 2^(E+1))
+  double r = std::rint(std::ldexp(a, 10 - E));  // in [1024, 2048]
+  if (r == 2048.0) {
+    r = 1024.0;
+    E += 1;
+  }
+  if (E > 15) return sign | 0x7C00;  // overflow to infinity
+  return sign | static_cast<uint16_t>(((E + 15) << 10) | (static_cast<int>(r) - 1024));
+}
+
+double bf16_to_double(uint16_t h) {
+  const uint32_t bits = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return static_cast<double>(f);
+}
+
+uint16_t double_to_bf16(double x) {
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  if (std::isnan(x)) return sign | 0x7FC0;
+  const double a = std::fabs(x);
+  if (a == 0.0) return sign;
+  if (a < std::ldexp(1.0, -126)) {
+    const double q = std::rint(std::ldexp(a, 133));  // multiples of 2^-133
+    return sign | static_cast<uint16_t>(q);
+  }
+  int e2;
+  std::frexp(a, &e2);
+  int E = e2 - 1;
+  double r = std::rint(std::ldexp(a, 7 - E));  // in [128, 256]
+  if (r == 256.0) {
+    r = 128.0;
+    E += 1;
+  }
+  if (E > 127) return sign | 0x7F80;
+  return sign | static_cast<uint16_t>(((E + 127) << 7) | (static_cast<int>(r) - 128));
+}
+
+double load_elem(const void* base, int dtype, int64_t i) {
+  switch (dtype) {
+    case DT_F32: return static_cast<double>(static_cast<const float*>(base)[i]);
+    case DT_F16: return half_to_double(static_cast<const uint16_t*>(base)[i]);
+    default: return bf16_to_double(static_cast<const uint16_t*>(base)[i]);
+  }
+}
+
+void store_elem(void* base, int dtype, int64_t i, double v) {
+  switch (dtype) {
+    case DT_F32: static_cast<float*>(base)[i] = static_cast<float>(v); break;  // C cast: RNE
+    case DT_F16: static_cast<uint16_t*>(base)[i] = double_to_half(v); break;
+    default: static_cast<uint16_t*>(base)[i] = double_to_bf16(v); break;
+  }
+}
+
+struct Pair {
+  int64_t key;  // linear index
+  int64_t id;   // lookup id (position in indices)
+};
+
+// Steps 1-2. Also records the bag of every lookup. Returns a status code.
+int linearise_and_sort(int32_t T, int32_t B, const int64_t* hsc, const int64_t* indices,
+                       const int64_t* offsets, int64_t N, std::vector<Pair>* pairs,
+                       std::vector<int64_t>* bag_of) {
+  if (T <= 0 || B <= 0 || N < 0) return ERR_INVALID_ARG;
+  if (offsets[0] != 0 || offsets[static_cast<int64_t>(B) * T] != N) return ERR_INVALID_ARG;
+  pairs->clear();
+  pairs->reserve(static_cast<size_t>(N));
+  bag_of->assign(static_cast<size_t>(N), -1);
+  for (int64_t bt = 0; bt < static_cast<int64_t>(B) * T; ++bt) {
+    if (offsets[bt + 1] < offsets[bt]) return ERR_INVALID_ARG;
+    const int64_t t = bt / B;
+    const int64_t rows = hsc[t + 1] - hsc[t];
+    for (int64_t i = offsets[bt]; i < offsets[bt + 1]; ++i) {
+      if (indices[i] < 0 || indices[i] >= rows) return ERR_INDEX_OUT_OF_RANGE;
+      pairs->push_back(Pair{hsc[t] + indices[i], i});
+      (*bag_of)[i] = bt;
+    }
+  }
+  std::sort(pairs->begin(), pairs->end(), [](const Pair& a, const Pair& b) {
+    return a.key != b.key ? a.key < b.key : a.id < b.id;
+  });
+  return OK;
+}
+
+int32_t table_of_key(int32_t T, const int64_t* hsc, int64_t key) {
+  int32_t t = 0;
+  while (t + 1 < T && hsc[t + 1] <= key) ++t;
+  return t;
+}
+
+struct Runs {
+  std::vector<int64_t> keys;
+  std::vector<int64_t> start;  // start[r] = first position of run r; start[U] = N
+};
+
+Runs encode_runs(const std::vector<Pair>& pairs) {
+  Runs R;
+  for (size_t i = 0; i < pairs.size(); ++i) {
+    if (i == 0 || pairs[i].key != pairs[i - 1].key) {
+      R.keys.push_back(pairs[i].key);
+      R.start.push_back(static_cast<int64_t>(i));
+    }
+  }
+  R.start.push_back(static_cast<int64_t>(pairs.size()));
+  return R;
+}
+
+bool valid_tables(int32_t T, const int64_t* hsc, const int32_t* D_offsets) {
+  if (hsc[0] != 0) return false;
+  for (int32_t t = 0; t < T; ++t) {
+    if (hsc[t + 1] <= hsc[t]) return false;  // disjoint, non-empty tables
+    if (D_offsets && D_offsets[t + 1] <= D_offsets[t]) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Linearise + sort: sorted (key, lookup id) pairs. keys/ids have capacity N.
+int oracle_sorted_pairs(int32_t T, int32_t B, const int64_t* hsc, const int64_t* indices,
+                        const int64_t* offsets, int64_t N, int64_t* keys, int64_t* ids) {
+  std::vector<Pair> pairs;
+  std::vector<int64_t> bag_of;
+  const int st = linearise_and_sort(T, B, hsc, indices, offsets, N, &pairs, &bag_of);
+  if (st != OK) return st;
+  for (int64_t i = 0; i < N; ++i) {
+    keys[i] = pairs[i].key;
+    ids[i] = pairs[i].id;
+  }
+  return OK;
+}
+
+// Integer outputs of the sort / run-length / long-segment steps.
+//   run_keys[U]  ascending unique linear indices
+//   run_len[U]   lookups per unique index
+//   cum[U+1]     exclusive scan of run_len (cum[0] = 0, cum[U] = N)
+//   long_ids[..] run ids with run_len >= max_segment_length_per_warp, ascending
+// Output arrays have capacity N (cum: N + 1).
+int oracle_runs(int32_t T, int32_t B, const int64_t* hsc, const int64_t* indices,
+                const int64_t* offsets, int64_t N, int32_t max_segment_length_per_warp,
+                int64_t* run_keys, int32_t* run_len, int32_t* cum, int64_t* num_runs,
+                int32_t* long_ids, int64_t* num_long) {
+  std::vector<Pair> pairs;
+  std::vector<int64_t> bag_of;
+  const int st = linearise_and_sort(T, B, hsc, indices, offsets, N, &pairs, &bag_of);
+  if (st != OK) return st;
+  const Runs R = encode_runs(pairs);
+  const int64_t U = static_cast<int64_t>(R.keys.size());
+  int64_t nl = 0;
+  for (int64_t r = 0; r < U; ++r) {
+    run_keys[r] = R.keys[r];
+    run_len[r] = static_cast<int32_t>(R.start[r + 1] - R.start[r]);
+    cum[r] = static_cast<int32_t>(R.start[r]);
+    if (run_len[r] >= max_segment_length_per_warp) long_ids[nl++] = static_cast<int32_t>(r);
+  }
+  cum[U] = static_cast<int32_t>(N);
+  *num_runs = U;
+  *num_long = nl;
+  return OK;
+}
+
+// Step 4: de-duplicated row gradients, in double.
+//   nobag == 0: grad_output is [B, D_offsets[T]] and lookup i of bag (t, b)
+//               contributes scale_i * grad_output[b, D_offsets[t] : D_offsets[t+1]].
+//   nobag != 0: grad_output is [N, D] (all tables share D) and lookup l
+//               contributes grad_output[l, :].
+// Outputs: keys_out[U] and G[U * Dmax] (row r at G + r*Dmax, zero padded).
+int oracle_row_grads(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_offsets,
+                     const int64_t* indices, const int64_t* offsets, int64_t N,
+                     const float* per_sample_weights, int32_t mean_pooling, int32_t nobag,
+                     int32_t grad_dtype, const void* grad_output, int32_t Dmax,
+                     int64_t* keys_out, double* G, int64_t* num_rows) {
+  if (!valid_tables(T, hsc, D_offsets)) return ERR_INVALID_ARG;
+  if (nobag && per_sample_weights) return ERR_UNSUPPORTED;  // weighted nobag is not defined
+  if (nobag) {
+    for (int32_t t = 1; t < T; ++t)
+      if (D_offsets[t + 1] - D_offsets[t] != D_offsets[1] - D_offsets[0]) return ERR_INVALID_ARG;
+  }
+  std::vector<Pair> pairs;
+  std::vector<int64_t> bag_of;
+  const int st = linearise_and_sort(T, B, hsc, indices, offsets, N, &pairs, &bag_of);
+  if (st != OK) return st;
+  const Runs R = encode_runs(pairs);
+  const int64_t U = static_cast<int64_t>(R.keys.size());
+  const int64_t row_stride = D_offsets[T];
+  for (int64_t r = 0; r < U; ++r) {
+    const int32_t t = table_of_key(T, hsc, R.keys[r]);
+    const int32_t D = D_offsets[t + 1] - D_offsets[t];
+    if (D > Dmax) return ERR_INVALID_ARG;
+    double* g = G + r * static_cast<int64_t>(Dmax);
+    for (int32_t d = 0; d < Dmax; ++d) g[d] = 0.0;
+    for (int64_t j = R.start[r]; j < R.start[r + 1]; ++j) {
+      const int64_t i = pairs[j].id;
+      if (nobag) {
+        for (int32_t d = 0; d < D; ++d) g[d] += load_elem(grad_output, grad_dtype, i * D + d);
+      } else {
+        const int64_t bt = bag_of[i];
+        const int64_t b = bt % B;
+        double s = per_sample_weights ? static_cast<double>(per_sample_weights[i]) : 1.0;
+        if (mean_pooling) {
+          const int64_t L = offsets[bt + 1] - offsets[bt];  // >= 1: the bag holds lookup i
+          s *= 1.0 / static_cast<double>(L);
+        }
+        const int64_t base = b * row_stride + D_offsets[t];
+        for (int32_t d = 0; d < D; ++d) g[d] += s * load_elem(grad_output, grad_dtype, base + d);
+      }
+    }
+    keys_out[r] = R.keys[r];
+  }
+  *num_rows = U;
+  return OK;
+}
+
+// Step 5-6 on one row: applies the optimizer to row `w` (storage dtype) of
+// length D with gradient g (double) and, for row-wise Adagrad, the fp32 state m.
+//   optimizer 0 = SGD, 1 = row-wise Adagrad.
+int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int64_t row_offset,
+                     int32_t D, const double* g, float* m, double lr, double eps) {
+  if (optimizer == 0) {
+    for (int32_t d = 0; d < D; ++d) {
+      const double w = load_elem(weights, weight_dtype, row_offset + d);
+      store_elem(weights, weight_dtype, row_offset + d, w - lr * g[d]);
+    }
+    return OK;
+  }
+  if (optimizer != 1 || !m) return ERR_INVALID_ARG;
+  double sum_sq = 0.0;
+  for (int32_t d = 0; d < D; ++d) sum_sq += g[d] * g[d];
+  const double m_new = static_cast<double>(*m) + sum_sq / static_cast<double>(D);
+  const double mult = lr / (std::sqrt(m_new) + eps);
+  for (int32_t d = 0; d < D; ++d) {
+    const double w = load_elem(weights, weight_dtype, row_offset + d);
+    store_elem(weights, weight_dtype, row_offset + d, w - mult * g[d]);
+  }
+  *m = static_cast<float>(m_new);
+  return OK;
+}
+
+// The whole pooled (nobag == 0) or unpooled (nobag != 0) backward with the
+// optimizer applied in place to each unique touched row. Untouched rows are
+// not written. momentum_offsets may be NULL (then row idx of table t uses
+// momentum[hash_size_cumsum[t] + idx]); momentum is ignored for SGD.
+int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_offsets,
+                    const int64_t* weights_offsets, const int64_t* momentum_offsets,
+                    int32_t weight_dtype, void* weights, float* momentum,
+                    const int64_t* indices, const int64_t* offsets, int64_t N,
+                    const float* per_sample_weights, int32_t mean_pooling, int32_t nobag,
+                    int32_t grad_dtype, const void* grad_output, int32_t optimizer, double lr,
+                    double eps) {
+  if (T <= 0 || B <= 0) return ERR_INVALID_ARG;
+  if (N == 0) return OK;
+  int32_t Dmax = 0;
+  for (int32_t t = 0; t < T; ++t) Dmax = std::max(Dmax, D_offsets[t + 1] - D_offsets[t]);
+  std::vector<int64_t> keys(static_cast<size_t>(N));
+  std::vector<double> G(static_cast<size_t>(N) * static_cast<size_t>(Dmax));
+  int64_t U = 0;
+  const int st = oracle_row_grads(T, B, hsc, D_offsets, indices, offsets, N, per_sample_weights,
+                                  mean_pooling, nobag, grad_dtype, grad_output, Dmax, keys.data(),
+                                  G.data(), &U);
+  if (st != OK) return st;
+  for (int64_t r = 0; r < U; ++r) {
+    const int32_t t = table_of_key(T, hsc, keys[r]);
+    const int64_t idx = keys[r] - hsc[t];
+    const int32_t D = D_offsets[t + 1] - D_offsets[t];
+    float* m = nullptr;
+    if (optimizer == 1) {
+      const int64_t mo = momentum_offsets ? momentum_offsets[t] : hsc[t];
+      m = momentum + mo + idx;
+    }
+    const int st2 = oracle_apply_row(optimizer, weight_dtype, weights, weights_offsets[t] + idx * D,
+                                     D, G.data() + r * static_cast<int64_t>(Dmax), m, lr, eps);
+    if (st2 != OK) return st2;
+  }
+  return OK;
+}
+
+// Storage conversions, exported for the pin tests.
+uint16_t oracle_double_to_half(double x) { return double_to_half(x); }
+double oracle_half_to_double(uint16_t h) { return half_to_double(h); }
+uint16_t oracle_double_to_bf16(double x) { return double_to_bf16(x); }
+double oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
+
+}  // extern "C"
