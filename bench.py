@@ -1,0 +1,404 @@
+"""Benchmark: embedding backward + fused optimizer step through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dlrm|tiny|mixed|lm|large] [--no-cpu-baseline]
+
+One step = one whole pass of the hot path (linearise, sort, run-length encode,
+long-run partition, fused reduce + optimizer) over one synthetic batch. The
+default workload is the DLRM-like one (8 tables x 100k rows, D=64 fp32, B=2048,
+bag length U{1..20}, Zipf(1.05) ids, row-wise Adagrad). Its working set is far
+below L2, so a 256 MB buffer is written between timed steps to flush L2.
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own batch on
+its own GPU (weak scaling, no collective: tables are independent).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "embedding bwd+update: lookups/sec and achieved HBM GB/s vs GB300 peak"
+DESCR = {
+    "dlrm": "DLRM-like: T=8 x 100k rows, D=64 fp32, B=2048, L~U{1..20}, Zipf(1.05) ids, sum, "
+            "row-wise Adagrad lr=0.01 eps=1e-8",
+    "tiny": "tiny pooled: T=2 (1000, 500 rows), D=16 fp32, B=64, L~U{0..4}, uniform ids, sum, SGD",
+    "mixed": "mixed tables: T=26, rows log-uniform 1e3..1e6, D in {32,64,128,256}, fp16 weights, "
+             "fp32 grad, B=16384, L~Poisson(15), weighted, mean, row-wise Adagrad",
+    "lm": "unpooled LM: vocab 128256, D=4096 fp32 weights, bf16 grad, 32768 tokens, Zipf(1.1), SGD",
+    "large": "large skewed: T=64 x 2M rows, D=128 fp16 weights, B=65536, L power law mean 30 max 500, "
+             "Zipf(1.2) ids, sum, row-wise Adagrad",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dlrm", choices=list(DESCR))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "sorted", "atomic"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def make_workload(name, seed, device):
+    from sparse_embedding_bag_gb300 import synth
+    if name == "large":
+        return synth.large_on_device(seed, device=device)
+    return synth.BY_NAME[name](seed)
+
+
+def host_arrays(w):
+    """Host copies of a workload's step inputs (device-drawn workloads are copied back)."""
+    import torch
+    conv = lambda x: None if x is None else (x.cpu().numpy() if isinstance(x, torch.Tensor) else x)
+    return conv(w.indices), conv(w.offsets), conv(w.grad_output), conv(w.per_sample_weights)
+
+
+def algorithmic_bytes(w, indices, offsets):
+    """Minimal bytes of one step: int64 indices, the gradient row read per lookup,
+    and one read + one write of every unique row (and its fp32 state for Adagrad).
+    Returns (step bytes, reduce-kernel bytes, unique rows)."""
+    from sparse_embedding_bag_gb300 import synth
+    lengths = np.diff(offsets)
+    t_of_lookup = np.repeat(np.arange(w.T * w.B) // w.B, lengths)
+    keys = w.hash_size_cumsum[t_of_lookup] + indices
+    uniq = np.unique(keys)
+    t_of_row = np.searchsorted(w.hash_size_cumsum, uniq, side="right") - 1
+    gsize = 4 if w.grad_dtype == synth.F32 else 2
+    wsize = 4 if w.weight_dtype == synth.F32 else 2
+    grad_bytes = int(w.dims[t_of_lookup].astype(np.int64).sum()) * gsize
+    row_bytes = int(w.dims[t_of_row].astype(np.int64).sum()) * 2 * wsize
+    state = 8 * uniq.size if w.optimizer == synth.ROWWISE_ADAGRAD else 0
+    reduce_bytes = grad_bytes + row_bytes + state
+    return 8 * indices.size + reduce_bytes, reduce_bytes, int(uniq.size)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def cpu_baseline(w, budget_s):
+    """The oracle, as it stands (single thread), on the same workload for ~budget_s seconds."""
+    import oracle
+    from sparse_embedding_bag_gb300 import synth
+    indices, offsets, grad, psw = host_arrays(w)
+    n_done, el, runs = 0, 0.0, 0
+    while el < budget_s:
+        weights = np.array(w.weights, copy=True)
+        mom = None if w.momentum is None else np.array(w.momentum, copy=True)
+        t1 = time.perf_counter()
+        oracle.backward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, weights,
+                        indices, offsets, grad, optimizer=w.optimizer, lr=w.lr, eps=w.eps,
+                        momentum=mom, momentum_offsets=w.momentum_offsets, per_sample_weights=psw,
+                        mean=(w.pooling == synth.MEAN), nobag=w.nobag, grad_dtype=w.grad_dtype)
+        el += time.perf_counter() - t1
+        n_done += indices.size
+        runs += 1
+    return {"value": n_done / el, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+            "sample": f"{runs} full step(s) of the same workload ({indices.size} lookups each), "
+                      f"{el:.1f} s, single-threaded C++ oracle (double accumulation)"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle timed on the same workload, metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from sparse_embedding_bag_gb300 import synth
+    oracle.build()
+    w = make_workload(args.workload if args.workload != "large" else "dlrm", 0, "cpu")
+    indices, offsets, grad, psw = host_arrays(w)
+
+    def one():
+        weights = np.array(w.weights, copy=True)
+        mom = None if w.momentum is None else np.array(w.momentum, copy=True)
+        t = time.perf_counter()
+        oracle.backward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, weights,
+                        indices, offsets, grad, optimizer=w.optimizer, lr=w.lr, eps=w.eps,
+                        momentum=mom, momentum_offsets=w.momentum_offsets, per_sample_weights=psw,
+                        mean=(w.pooling == synth.MEAN), nobag=w.nobag, grad_dtype=w.grad_dtype)
+        return time.perf_counter() - t
+
+    for _ in range(args.warmup):
+        one()
+    times = [one() for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = indices.size / (ms / 1e3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "lookups/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": DESCR[args.workload if args.workload != "large" else "dlrm"],
+                                        "N": int(indices.size)},
+        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full steps, single-threaded C++ oracle"},
+        "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+
+    from sparse_embedding_bag_gb300 import build as b
+    from sparse_embedding_bag_gb300 import device as dev
+    from sparse_embedding_bag_gb300 import embbwd as E
+    from sparse_embedding_bag_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    b.build()
+    E.load()
+
+    w = make_workload(args.workload, rank, f"cuda:{local}")
+    indices_h, offsets_h, grad_h, psw_h = host_arrays(w)
+    step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, indices_h, offsets_h)
+    dw = dev.to_device(w, f"cuda:{local}")
+    plan = dev.make_plan(w, device_index=local)
+    path = {"auto": E.EMB_NOBAG_AUTO, "sorted": E.EMB_NOBAG_SORTED, "atomic": E.EMB_NOBAG_ATOMIC}[args.path]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=f"cuda:{local}")
+
+    def call():
+        dev.step(plan, dw, path=path)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    st = E.emb_plan_status(plan)
+    if st != E.EMB_OK:
+        raise SystemExit(f"device status {E.status_string(st)}")
+
+    use_graph = not args.no_graph
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def one_step():
+        graph.replay() if use_graph else call()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(K):
+            flush.zero_()
+            starts[k].record()
+            one_step()
+            ends[k].record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_list = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(ms_list) / K
+    st = E.emb_plan_status(plan)
+    if st != E.EMB_OK:
+        raise SystemExit(f"device status {E.status_string(st)}")
+    n_local = int(indices_h.size)
+    if world > 1:
+        t = torch.tensor([ms, float(n_local)], device=f"cuda:{local}", dtype=torch.float64)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        ms_job, n_job = float(mx[0]), float(sm[1])
+    else:
+        ms_job, n_job = ms, float(n_local)
+
+    # ---- per-stage times (profiled replays, same work) -> dominant kernel roofline
+    E.emb_plan_set_profiling(plan, True)
+    stage_runs = []
+    if use_graph:
+        gprof = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gprof):
+            call()
+        run_prof = gprof.replay
+    else:
+        run_prof = call
+    for k in range(K):
+        flush.zero_()
+        run_prof()
+        torch.cuda.synchronize()
+        stage_runs.append(E.emb_plan_stage_ms(plan))
+    E.emb_plan_set_profiling(plan, False)
+    stage = np.mean(np.array(stage_runs), axis=0)
+    names = ["linearise_hist", "radix_sort", "run_length", "long_partition", "reduce_update"]
+    if w.nobag and path == E.EMB_NOBAG_ATOMIC:
+        names = ["index_check", "-", "-", "-", "atomic_scatter"]
+    dom = int(np.argmax(stage))
+    peak, peak_kind = peaks()
+    total_bits = int(np.ceil(np.log2(max(int(w.hash_size_cumsum[-1]), 2))))
+    passes = (total_bits + 7) // 8
+    vbytes = 8 if (w.per_sample_weights is not None or w.pooling == synth.MEAN) else 4
+    N = n_local
+    stage_bytes = {
+        "linearise_hist": 8 * N + 8 * (w.T * w.B + 1),
+        "radix_sort": N * (8 + 4 + vbytes) + (passes - 1) * N * 2 * (4 + vbytes),
+        "run_length": 4 * N + 8 * uniq,
+        "long_partition": 8 * uniq,
+        "reduce_update": reduce_bytes,
+        "index_check": 8 * N,
+        "atomic_scatter": reduce_bytes,
+    }
+    dom_name = names[dom]
+    achieved = stage_bytes.get(dom_name, 0) / (stage[dom] * 1e-3) / 1e9
+    red_achieved = reduce_bytes / (stage[4] * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers (H2D + call + status read)
+    pin = lambda a: None if a is None else torch.from_numpy(
+        np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+    h_idx, h_off, h_grad, h_psw = pin(indices_h), pin(offsets_h), pin(grad_h), pin(psw_h)
+    h2d = sum(x.numel() * x.element_size() for x in (h_idx, h_off, h_grad, h_psw) if x is not None)
+    e2e_times = []
+    for k in range(max(3, K // 2) + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dw.indices.copy_(h_idx, non_blocking=True)
+        dw.offsets.copy_(h_off, non_blocking=True)
+        dw.grad_output.copy_(h_grad, non_blocking=True)
+        if h_psw is not None:
+            dw.per_sample_weights.copy_(h_psw, non_blocking=True)
+        call()
+        st = E.emb_plan_status(plan)  # waits and reads the 4-byte status word back
+        e2e_times.append(time.perf_counter() - t0)
+        if st != E.EMB_OK:
+            raise SystemExit(f"device status {E.status_string(st)}")
+    e2e_s = statistics.median(e2e_times[2:])
+    e2e_val = n_local / e2e_s
+    if world > 1:
+        t = torch.tensor([e2e_s], device=f"cuda:{local}", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_val = n_job / float(t[0])
+
+    kernels_per_step = 2 if (w.nobag and path == E.EMB_NOBAG_ATOMIC) else 4 + passes
+    result = {
+        "metric": METRIC,
+        "value": n_job / (ms_job * 1e-3),
+        "unit": "lookups/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_job,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "N": n_local, "unique_rows": uniq,
+                   "l2": "256 MB buffer written between timed steps", "cuda_graph": use_graph,
+                   "parallelism": f"{world} independent shard(s), no collective"},
+        "hbm_gbs": step_bytes / (ms_job * 1e-3) / 1e9,
+        "step_bytes": step_bytes,
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None},
+        "reduce_update": {"ms": float(stage[4]), "gbs": red_achieved, "frac": red_achieved / peak,
+                          "bytes": reduce_bytes},
+        "stage_ms": {n: float(v) for n, v in zip(names, stage) if n != "-"},
+        "e2e": {"value": e2e_val, "unit": "lookups/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": kernels_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    E.emb_plan_destroy(plan)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

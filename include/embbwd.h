@@ -1,0 +1,173 @@
+/*
+ * embbwd — backward pass of pooled (EmbeddingBag) and unpooled embedding
+ * lookups over many tables, with SGD or row-wise Adagrad applied in place to
+ * every unique touched row. GB300 (sm_103a) CUDA kernels behind a plain C ABI.
+ *
+ * The operation (the problem statement of "fbgemm_gpu/codegen/
+ * embedding_backward_split_template.cu", host function
+ * split_embedding_backward_codegen_{optimizer}_{weighted}_exact_cuda):
+ *
+ *   For table t and bag b with lookups i in [offsets[t*B+b], offsets[t*B+b+1]):
+ *     G_t[indices[i]] += s_i * grad_output[b, D_offsets[t] : D_offsets[t+1]]
+ *   with s_i = per_sample_weights[i] (if given) * (1/L under mean pooling),
+ *   L the bag's length. Unpooled ("nobag"): G_t[indices[l]] += grad_output[l, :].
+ *   Then, once for every unique touched row (t, idx):
+ *     SGD:               w <- w - lr * G
+ *     row-wise Adagrad:  m <- m + sum_d(G_d^2)/D_t ;  w <- w - lr * G / (sqrt(m) + eps)
+ *   ("tt_embeddings_cuda.cu": update_tt_cores_sgd_kernel and
+ *    cache_backward_rowwise_adagrad_approx_kernel give the two update rules;
+ *    here they act on the de-duplicated row gradient.)
+ *   The update is computed in fp32 and rounded once (round-to-nearest-even)
+ *   to the weight's storage type. Rows that no lookup touches are not written.
+ *
+ * Layouts (all element offsets, not bytes):
+ *   weights        flat; row idx of table t starts at weights_offsets[t] + idx*D_t
+ *   momentum       fp32; row idx of table t at momentum_offsets[t] + idx
+ *                  (momentum_offsets NULL => hash_size_cumsum[t] + idx)
+ *   indices        int64[N], row ids local to their table
+ *   offsets        int64[B*T+1], CSR over bags in table-major order (bag t*B+b)
+ *   grad_output    pooled: [B, D_offsets[T]] row-major; unpooled: [N, D]
+ *   per_sample_weights  fp32[N] or NULL
+ *
+ * Ownership: every tensor pointer passed to a call is caller-owned device
+ * memory. Host arrays given to emb_bwd_plan are copied. The plan owns all of
+ * its scratch (device memory sized from max_N at plan time); calls allocate
+ * nothing.
+ *
+ * Execution: calls enqueue work on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) and return without synchronising. Argument errors are
+ * returned synchronously. Errors found on the device (an index outside its
+ * table, malformed offsets, a bounded wait that ran out) are latched in the
+ * plan, leave weights and momentum unmodified, and are returned by the next
+ * emb_plan_status(). One plan serves one call at a time: calls on one plan
+ * must be ordered (same stream, or synchronised), because they share scratch.
+ * A call contains no host synchronisation and no allocation, so it can be
+ * captured in a CUDA graph.
+ */
+#ifndef EMBBWD_H
+#define EMBBWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EMB_OK = 0,
+  EMB_ERR_INVALID_ARG = 1,         /* bad argument, or malformed offsets found on the device */
+  EMB_ERR_UNSUPPORTED = 2,         /* valid but not supported by this build (see each call) */
+  EMB_ERR_INDEX_OUT_OF_RANGE = 3,  /* an index outside [0, rows of its table) */
+  EMB_ERR_OOM = 4,                 /* plan scratch could not be allocated */
+  EMB_ERR_CUDA = 5,                /* a CUDA runtime call failed */
+  EMB_ERR_TIMEOUT = 6              /* a bounded inter-block wait ran out; nothing was updated */
+} emb_status;
+
+typedef enum { EMB_F32 = 0, EMB_F16 = 1, EMB_BF16 = 2 } emb_dtype;
+typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pooling;
+typedef enum { EMB_NOBAG_AUTO = 0, EMB_NOBAG_SORTED = 1, EMB_NOBAG_ATOMIC = 2 } emb_nobag_path;
+
+/* emb_bwd_plan flags. Index range checking is always on. */
+#define EMB_FLAG_CHECK_INDICES 0x1u
+/* Test only: every block that would wait on another one gives up at once and
+ * reports EMB_ERR_TIMEOUT, exercising the error path without a real stall. */
+#define EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u
+
+typedef struct emb_plan emb_plan;
+
+/* Creates a plan for a fixed set of tables.
+ *   device            CUDA device ordinal the plan and all its calls use.
+ *   T                 number of tables, 1..4096.
+ *   hash_size_cumsum  host int64[T+1]: hash_size_cumsum[t] = rows of tables < t;
+ *                     strictly increasing, hash_size_cumsum[0] = 0, total rows < 2^32.
+ *                     Row idx of table t has linear index hash_size_cumsum[t] + idx
+ *                     ("embedding_backward_split_template.cu", the per-row kernels).
+ *   D_offsets         host int32[T+1]: D_t = D_offsets[t+1] - D_offsets[t], each a
+ *                     positive multiple of 4 (the pages' vector width) and <= 4096.
+ *   weights_offsets   host int64[T], each a multiple of 4.
+ *   momentum_offsets  host int64[T] or NULL.
+ *   weight_dtype      storage type of weights (fp32, fp16, bf16).
+ *   grad_dtype        type of grad_output (fp32, fp16, bf16).
+ *   max_N             largest lookup count any call will pass (< 2^30).
+ *   max_B             largest batch any call will pass (max_B * T < 2^31).
+ *   max_segment_length_per_warp  runs at least this long take the block-level
+ *                     path ("embedding_backward_split_template.cu",
+ *                     *_find_long_segments); <= 0 selects 32.
+ *   flags             EMB_FLAG_* bits.
+ * Returns EMB_ERR_INVALID_ARG for malformed arguments, EMB_ERR_OOM if scratch
+ * cannot be allocated, EMB_ERR_CUDA on other runtime failures. *out is NULL on error. */
+emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* hash_size_cumsum,
+                        const int32_t* D_offsets, const int64_t* weights_offsets,
+                        const int64_t* momentum_offsets, emb_dtype weight_dtype,
+                        emb_dtype grad_dtype, int64_t max_N, int32_t max_B,
+                        int32_t max_segment_length_per_warp, uint32_t flags);
+
+/* Frees the plan and its scratch (synchronises the device). NULL is accepted. */
+emb_status emb_plan_destroy(emb_plan* plan);
+
+/* Pooled backward + SGD, in place on `weights` (plan's weight_dtype).
+ * offsets has B*T+1 entries with offsets[0] = 0 and offsets[B*T] = N; B <= max_B,
+ * N <= max_N. per_sample_weights may be NULL. N = 0 returns EMB_OK and does nothing
+ * ("embedding_backward_split_template.cu": the exact_cuda host function's
+ * empty-indices short-circuit and its T > 0, B > 0 checks). */
+emb_status emb_bag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indices,
+                           const int64_t* offsets, int64_t N, int32_t B,
+                           const float* per_sample_weights, const void* grad_output,
+                           emb_pooling mode, float lr, void* stream);
+
+/* Pooled backward + row-wise Adagrad, in place on `weights` and fp32 `momentum`.
+ * Same arguments as emb_bag_bwd_sgd plus momentum and eps. Requires every D_t <= 1024
+ * (one warp holds the whole row for the row-wise norm); otherwise EMB_ERR_UNSUPPORTED. */
+emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* plan, void* weights, float* momentum,
+                                       const int64_t* indices, const int64_t* offsets,
+                                       int64_t N, int32_t B, const float* per_sample_weights,
+                                       const void* grad_output, emb_pooling mode, float lr,
+                                       float eps, void* stream);
+
+/* Unpooled backward + SGD: lookup l adds grad_output[l, :] (shape [N, D], every
+ * table has the same D) to row indices[l] of its table, the table given by the
+ * CSR offsets (B*T+1 entries; only table membership matters). There is no
+ * weighted variant ("embedding_backward_split_template.cu" generates no
+ * weighted nobag kernel).
+ *   path EMB_NOBAG_SORTED: sort + de-duplicated, deterministic update.
+ *   path EMB_NOBAG_ATOMIC: one float atomic add of -lr*g per element, no sort
+ *        ("tinygrad/nn/__init__.py", _embedding_bwd_kernel; "tt_embeddings_cuda.cu",
+ *        cache_backward_sgd_kernel); fp32 weights only, else EMB_ERR_UNSUPPORTED.
+ *   path EMB_NOBAG_AUTO: the faster of the two for the plan's types. */
+emb_status emb_nobag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indices,
+                             const int64_t* offsets, int64_t N, int32_t B,
+                             const void* grad_output, float lr, emb_nobag_path path,
+                             void* stream);
+
+/* Waits for the plan's last call, then returns and clears the latched device
+ * error (EMB_OK if none). */
+emb_status emb_plan_status(emb_plan* plan);
+
+/* Host copies of the last sorted call's integer outputs, for parity checks:
+ * run_keys (ascending unique linear indices), run_len, cum (exclusive scan of
+ * run_len, num_runs+1 entries), num_runs, long_ids (runs with run_len >=
+ * max_segment_length_per_warp; the order is unspecified, compare as a set) and
+ * num_long. Arrays need `capacity` entries (cum: capacity+1); any pointer may be
+ * NULL. Synchronises. EMB_ERR_INVALID_ARG if the last call was not a sorted one or
+ * a count exceeds capacity. */
+emb_status emb_plan_debug_runs(emb_plan* plan, int64_t capacity, int64_t* run_keys,
+                               int32_t* run_len, int32_t* cum, int32_t* num_runs,
+                               int32_t* long_ids, int32_t* num_long);
+
+/* Profiling: when enabled, calls record CUDA events between their stages. */
+emb_status emb_plan_set_profiling(emb_plan* plan, int enable);
+
+/* Stage durations (ms) of the last profiled call; synchronises. Sorted path:
+ * [0] linearise + histogram, [1] radix sort passes, [2] run-length encode,
+ * [3] long-run partition, [4] reduce + optimizer. Atomic path: [0] index check,
+ * [4] atomic scatter, others 0. Writes min(n, 5) values. */
+emb_status emb_plan_stage_ms(emb_plan* plan, float* ms, int32_t n);
+
+/* Static description of a status code. */
+const char* emb_status_string(emb_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMBBWD_H */

@@ -1,0 +1,583 @@
+// C ABI of libembbwd: argument validation, plan (scratch) management and the
+// per-call launch sequence. Host code only; the kernels live in the other
+// translation units. The host layer mirrors the checks of the exact_cuda host
+// function of "fbgemm_gpu/codegen/embedding_backward_split_template.cu"
+// (T > 0, B > 0, the embedding-dimension limit, the empty-indices
+// short-circuit) and adds the alignment and capacity checks the vectorised
+// kernels need.
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/embbwd.h"
+#include "internal.cuh"
+
+using namespace embbwd;
+
+namespace {
+
+constexpr uint32_t kSpinLimit = 1u << 22;  // polls before a look-back wait gives up (~1 s)
+constexpr uint32_t kPart = 1024;           // lookups per block work item of a long run
+constexpr int kStages = 5;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct emb_plan {
+  int device = 0;
+  int32_t T = 0;
+  emb_dtype wdt = EMB_F32, gdt = EMB_F32;
+  int64_t max_N = 0;
+  int32_t max_B = 0;
+  uint32_t thr = 32;
+  uint32_t flags = 0;
+  int max_D = 0;
+  bool uniform_D = true;
+  int kv = 1;
+  uint32_t C = 1;
+  int key_bits = 1;
+  std::vector<uint32_t> hsc;
+  std::vector<int32_t> Do;
+  DevProps props{};
+
+  void* arena = nullptr;
+  Ctl* ctl = nullptr;
+  uint32_t* sticky = nullptr;
+  uint32_t* d_hsc = nullptr;
+  int32_t* d_Do = nullptr;
+  int64_t* d_wo = nullptr;
+  int64_t* d_mo = nullptr;
+  uint32_t* keys[2] = {nullptr, nullptr};
+  void* vals[2] = {nullptr, nullptr};
+  uint64_t* status = nullptr;
+  uint32_t* run_key = nullptr;
+  uint32_t* run_start = nullptr;
+  uint32_t* long_ids = nullptr;
+  uint32_t* item_base = nullptr;
+  uint32_t* slot_base = nullptr;
+  uint32_t* item_long = nullptr;
+  float4* partials = nullptr;
+  uint32_t* done = nullptr;
+  uint32_t cap_long = 0, cap_items = 0, cap_slots = 0;
+
+  uint32_t seq = 0;
+  int reduce_grid[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  cudaStream_t last_stream = nullptr;
+  int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
+  int64_t last_N = 0;
+
+  bool profiling = false;
+  bool events_ready = false;
+  cudaEvent_t ev[kStages + 1] = {};
+  int last_profiled = 0;  // 0 none, 1 sorted, 2 atomic
+};
+
+namespace {
+
+const void* reduce_fn(const emb_plan* p, int opt, int vk) {
+  ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->kv};
+  switch (p->wdt) {
+    case EMB_F32: return reduce_kernel_f32(k);
+    case EMB_F16: return reduce_kernel_f16(k);
+    default: return reduce_kernel_bf16(k);
+  }
+}
+
+emb_status record(emb_plan* p, int i, cudaStream_t s) {
+  if (!p->profiling) return EMB_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return EMB_ERR_CUDA;
+  const cudaError_t e = cs == cudaStreamCaptureStatusActive
+                            ? cudaEventRecordWithFlags(p->ev[i], s, cudaEventRecordExternal)
+                            : cudaEventRecord(p->ev[i], s);
+  return e == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+size_t dtype_size(emb_dtype d) { return d == EMB_F32 ? 4 : 2; }
+
+emb_status check_common(const emb_plan* p, const void* weights, const int64_t* indices,
+                        const int64_t* offsets, int64_t N, int32_t B, const void* grad) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  if (N < 0 || N > p->max_N || B <= 0 || B > p->max_B) return EMB_ERR_INVALID_ARG;
+  if (N == 0) return EMB_OK;
+  if (!weights || !indices || !offsets || !grad) return EMB_ERR_INVALID_ARG;
+  if (!aligned(weights, 4 * dtype_size(p->wdt)) || !aligned(grad, 4 * dtype_size(p->gdt)) ||
+      !aligned(indices, 8) || !aligned(offsets, 8))
+    return EMB_ERR_INVALID_ARG;
+  return EMB_OK;
+}
+
+DecodeArgs decode_args(const emb_plan* p, const int64_t* indices, const int64_t* offsets,
+                       const float* psw, int64_t N, int32_t B, int mean) {
+  DecodeArgs d;
+  d.indices = indices;
+  d.offsets = offsets;
+  d.psw = psw;
+  d.hsc = p->d_hsc;
+  d.N = N;
+  d.B = (uint32_t)B;
+  d.T = (uint32_t)p->T;
+  d.BT = (uint32_t)B * (uint32_t)p->T;
+  d.invB = 1.0f / (float)B;
+  d.mean = mean;
+  return d;
+}
+
+emb_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return EMB_OK;
+  cudaGetLastError();  // clear a sticky launch error
+  return e == cudaErrorMemoryAllocation ? EMB_ERR_OOM : EMB_ERR_CUDA;
+}
+
+#define EMB_TRY(expr)                     \
+  do {                                    \
+    const emb_status _st = (expr);        \
+    if (_st != EMB_OK) return _st;        \
+  } while (0)
+#define EMB_CUDA(expr) EMB_TRY(cuda_status(expr))
+
+// Sorted path: linearise + sort + run-length + long partition + fused reduce/update.
+emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* momentum,
+                      const int64_t* indices, const int64_t* offsets, int64_t N, int32_t B,
+                      const float* psw, const void* grad, int mean, float lr, float eps,
+                      cudaStream_t s) {
+  const uint32_t epoch = ++p->seq * 8u;
+  if (p->seq >= (1u << 28)) p->seq = 0;  // epochs stay distinct from the zero-initialised words
+  const DecodeArgs d = decode_args(p, indices, offsets, psw, N, B, mean);
+  const int tile = (int)sort_tile_for(N);
+  const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
+  const bool wide = vk == VK_BAG_SCALED;
+  const LookbackCfg lb0{p->status, epoch, kSpinLimit, (p->flags & EMB_FLAG_DEBUG_FORCE_TIMEOUT) ? 1u : 0u};
+
+  EMB_TRY(record(p, 0, s));
+  EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
+  HistArgs ha{d, p->ctl, p->sticky, passes, tile};
+  EMB_CUDA(launch_hist(ha, p->T, s));
+  EMB_TRY(record(p, 1, s));
+  for (int pass = 0; pass < passes; ++pass) {
+    PassArgs pa;
+    pa.d = d;
+    pa.ctl = p->ctl;
+    pa.sticky = p->sticky;
+    pa.lb = lb0;
+    pa.lb.epoch = epoch + (uint32_t)pass;
+    const int in = (pass + 1) & 1, out = pass & 1;
+    pa.keys_in = p->keys[in];
+    pa.vals_in = p->vals[in];
+    pa.keys_out = p->keys[out];
+    pa.vals_out = p->vals[out];
+    pa.pass = pass;
+    pa.shift = pass * kRadixBits;
+    EMB_CUDA(launch_sort_pass(pa, pass == 0 ? vk : -1, wide, tile, p->T, s));
+  }
+  const int fin = (passes - 1) & 1;
+  EMB_TRY(record(p, 2, s));
+  RleArgs ra{p->keys[fin], N, p->ctl, p->sticky, lb0, p->run_key, p->run_start};
+  ra.lb.epoch = epoch + 5;
+  EMB_CUDA(launch_rle(ra, s));
+  EMB_TRY(record(p, 3, s));
+  LongArgs la;
+  la.ctl = p->ctl;
+  la.sticky = p->sticky;
+  la.lb = lb0;
+  la.lb.epoch = epoch + 6;
+  la.run_start = p->run_start;
+  la.thr = p->thr;
+  la.part = kPart;
+  la.long_ids = p->long_ids;
+  la.item_base = p->item_base;
+  la.slot_base = p->slot_base;
+  la.item_long = p->item_long;
+  la.cap_long = p->cap_long;
+  la.cap_items = p->cap_items;
+  la.cap_slots = p->cap_slots;
+  const int64_t long_tiles = (N + kLongTile - 1) / kLongTile;
+  const int long_grid = (int)std::min<int64_t>(long_tiles, 2 * (int64_t)p->props.sms);
+  EMB_CUDA(launch_long(la, long_grid, s));
+  EMB_TRY(record(p, 4, s));
+
+  ReduceArgs r;
+  r.ctl = p->ctl;
+  r.vals = static_cast<const uint32_t*>(p->vals[fin]);
+  r.run_key = p->run_key;
+  r.run_start = p->run_start;
+  r.long_ids = p->long_ids;
+  r.item_base = p->item_base;
+  r.slot_base = p->slot_base;
+  r.item_long = p->item_long;
+  r.partials = p->partials;
+  r.done = p->done;
+  r.grad = grad;
+  r.weights = weights;
+  r.momentum = momentum;
+  r.hsc = p->d_hsc;
+  r.D_offsets = p->d_Do;
+  r.weights_offsets = p->d_wo;
+  r.momentum_offsets = p->d_mo;
+  r.T = (uint32_t)p->T;
+  r.B = (uint32_t)B;
+  r.grad_stride = vk == VK_NOBAG ? (int64_t)p->max_D : (int64_t)p->Do[p->T];
+  r.lr = lr;
+  r.eps = eps;
+  r.thr = p->thr;
+  r.part = kPart;
+  r.C = p->C;
+  const void* fn = reduce_fn(p, opt, vk);
+  if (!fn) return EMB_ERR_UNSUPPORTED;
+  void* args[] = {&r};
+  EMB_CUDA(cudaLaunchKernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads), args,
+                            reduce_smem_bytes(p->kv, p->T), s));
+  EMB_TRY(record(p, 5, s));
+  p->last_kind = 1;
+  p->last_N = N;
+  p->last_stream = s;
+  if (p->profiling) p->last_profiled = 1;
+  return EMB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* emb_status_string(emb_status st) {
+  switch (st) {
+    case EMB_OK: return "ok";
+    case EMB_ERR_INVALID_ARG: return "invalid argument";
+    case EMB_ERR_UNSUPPORTED: return "unsupported";
+    case EMB_ERR_INDEX_OUT_OF_RANGE: return "index out of range";
+    case EMB_ERR_OOM: return "out of device memory";
+    case EMB_ERR_CUDA: return "CUDA runtime error";
+    case EMB_ERR_TIMEOUT: return "bounded wait timed out";
+  }
+  return "unknown status";
+}
+
+emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* hash_size_cumsum,
+                        const int32_t* D_offsets, const int64_t* weights_offsets,
+                        const int64_t* momentum_offsets, emb_dtype weight_dtype,
+                        emb_dtype grad_dtype, int64_t max_N, int32_t max_B,
+                        int32_t max_segment_length_per_warp, uint32_t flags) {
+  if (!out) return EMB_ERR_INVALID_ARG;
+  *out = nullptr;
+  // ---- host-side validation (no CUDA call before this point)
+  if (T <= 0 || T > kMaxT || !hash_size_cumsum || !D_offsets || !weights_offsets)
+    return EMB_ERR_INVALID_ARG;
+  if (weight_dtype < EMB_F32 || weight_dtype > EMB_BF16 || grad_dtype < EMB_F32 || grad_dtype > EMB_BF16)
+    return EMB_ERR_INVALID_ARG;
+  if (max_N < 0 || max_N >= (int64_t)(1 << 30) || max_B <= 0 || (int64_t)max_B * T >= (int64_t)1 << 31)
+    return EMB_ERR_INVALID_ARG;
+  if (hash_size_cumsum[0] != 0 || D_offsets[0] != 0) return EMB_ERR_INVALID_ARG;
+  int max_D = 0;
+  bool uniform = true;
+  for (int32_t t = 0; t < T; ++t) {
+    if (hash_size_cumsum[t + 1] <= hash_size_cumsum[t]) return EMB_ERR_INVALID_ARG;
+    const int32_t D = D_offsets[t + 1] - D_offsets[t];
+    if (D <= 0 || D % 4 != 0 || D > 4096) return EMB_ERR_INVALID_ARG;
+    if (weights_offsets[t] < 0 || weights_offsets[t] % 4 != 0) return EMB_ERR_INVALID_ARG;
+    if (momentum_offsets && momentum_offsets[t] < 0) return EMB_ERR_INVALID_ARG;
+    if (D != D_offsets[1] - D_offsets[0]) uniform = false;
+    max_D = std::max(max_D, D);
+  }
+  if (hash_size_cumsum[T] > (int64_t)0xffffffffLL) return EMB_ERR_INVALID_ARG;
+
+  emb_plan* p = new (std::nothrow) emb_plan;
+  if (!p) return EMB_ERR_OOM;
+  p->device = device;
+  p->T = T;
+  p->wdt = weight_dtype;
+  p->gdt = grad_dtype;
+  p->max_N = max_N;
+  p->max_B = max_B;
+  p->thr = max_segment_length_per_warp > 0 ? (uint32_t)max_segment_length_per_warp : 32u;
+  p->flags = flags;
+  p->max_D = max_D;
+  p->uniform_D = uniform;
+  const int nvec = max_D / 4;
+  p->kv = nvec <= 32 ? 1 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
+  p->C = (uint32_t)((nvec + p->kv * 32 - 1) / (p->kv * 32));
+  const uint64_t total_rows = (uint64_t)hash_size_cumsum[T];
+  p->key_bits = 1;
+  while (p->key_bits < 32 && ((uint64_t)1 << p->key_bits) < total_rows) ++p->key_bits;
+  p->hsc.resize(T + 1);
+  p->Do.assign(D_offsets, D_offsets + T + 1);
+  for (int32_t t = 0; t <= T; ++t) p->hsc[t] = (uint32_t)hash_size_cumsum[t];
+
+  DeviceGuard g(device);
+  if (!g.ok) {
+    delete p;
+    return EMB_ERR_INVALID_ARG;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+    delete p;
+    return EMB_ERR_CUDA;
+  }
+  p->props.sms = prop.multiProcessorCount;
+  p->props.smem_optin = (int)prop.sharedMemPerBlockOptin;
+
+  // ---- scratch sizes
+  const uint64_t N = (uint64_t)std::max<int64_t>(max_N, 1);
+  const uint64_t sort_tiles = std::max<uint64_t>((N + 1023) / 1024, 1);  // smallest tile is 1024
+  const uint64_t status_words = std::max<uint64_t>(
+      sort_tiles * kRadix, std::max<uint64_t>((N + kRleTile - 1) / kRleTile, (N + kLongTile - 1) / kLongTile * 3));
+  p->cap_long = (uint32_t)(N / p->thr + 1);
+  p->cap_items = (uint32_t)(N / kPart + p->cap_long + 1);
+  p->cap_slots = (uint32_t)(2 * (N / kPart) + 2);
+  const size_t part_row = (size_t)p->kv * 32 * sizeof(float4);
+  struct Seg {
+    void** ptr;
+    size_t bytes;
+  };
+  void* tmp_ctl = nullptr;
+  void* tmp_sticky = nullptr;
+  Seg segs[] = {
+      {&tmp_ctl, sizeof(Ctl)},
+      {&tmp_sticky, sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->d_hsc), (T + 1) * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->d_Do), (T + 1) * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&p->d_wo), T * sizeof(int64_t)},
+      {reinterpret_cast<void**>(&p->d_mo), T * sizeof(int64_t)},
+      {reinterpret_cast<void**>(&p->keys[0]), N * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->keys[1]), N * sizeof(uint32_t)},
+      {&p->vals[0], N * sizeof(uint64_t)},
+      {&p->vals[1], N * sizeof(uint64_t)},
+      {reinterpret_cast<void**>(&p->status), status_words * sizeof(uint64_t)},
+      {reinterpret_cast<void**>(&p->run_key), N * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->item_base), p->cap_long * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->slot_base), p->cap_long * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->item_long), p->cap_items * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->partials), (size_t)p->cap_slots * p->C * part_row},
+      {reinterpret_cast<void**>(&p->done), (size_t)p->cap_slots * p->C * sizeof(uint32_t)},
+  };
+  size_t total = 0;
+  for (const Seg& sg : segs) total = align_up(total, 256) + sg.bytes;
+  if (cudaMalloc(&p->arena, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return EMB_ERR_OOM;
+  }
+  size_t off = 0;
+  for (const Seg& sg : segs) {
+    off = align_up(off, 256);
+    *sg.ptr = static_cast<char*>(p->arena) + off;
+    off += sg.bytes;
+  }
+  p->ctl = static_cast<Ctl*>(tmp_ctl);
+  p->sticky = static_cast<uint32_t*>(tmp_sticky);
+
+  std::vector<int64_t> mo(T);
+  for (int32_t t = 0; t < T; ++t) mo[t] = momentum_offsets ? momentum_offsets[t] : hash_size_cumsum[t];
+  cudaError_t e = cudaMemset(p->arena, 0, total);
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_hsc, p->hsc.data(), (T + 1) * sizeof(uint32_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_Do, D_offsets, (T + 1) * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_wo, weights_offsets, T * sizeof(int64_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_mo, mo.data(), T * sizeof(int64_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = sort_configure(p->props);
+  // Reduce kernels of this plan's types: shared-memory limit and persistent grid.
+  for (int opt = 0; opt < 2 && e == cudaSuccess; ++opt) {
+    for (int vk = 0; vk < 3 && e == cudaSuccess; ++vk) {
+      const void* fn = reduce_fn(p, opt, vk);
+      if (!fn) continue;
+      const size_t sm = reduce_smem_bytes(p->kv, T);
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      int blocks = 0;
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm);
+      p->reduce_grid[opt][vk] = std::max(blocks, 1) * p->props.sms;
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p->arena);
+    delete p;
+    return EMB_ERR_CUDA;
+  }
+  *out = p;
+  return EMB_OK;
+}
+
+emb_status emb_plan_destroy(emb_plan* p) {
+  if (!p) return EMB_OK;
+  DeviceGuard g(p->device);
+  cudaDeviceSynchronize();
+  if (p->events_ready)
+    for (cudaEvent_t ev : p->ev) cudaEventDestroy(ev);
+  const cudaError_t e = cudaFree(p->arena);
+  delete p;
+  return e == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
+}
+
+emb_status emb_bag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
+                           const int64_t* offsets, int64_t N, int32_t B,
+                           const float* per_sample_weights, const void* grad_output,
+                           emb_pooling mode, float lr, void* stream) {
+  EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
+  if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
+  if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
+  if (N == 0) {
+    p->last_kind = 0;
+    return EMB_OK;
+  }
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
+  return run_sorted(p, 0, vk, weights, nullptr, indices, offsets, N, B, per_sample_weights,
+                    grad_output, mode == EMB_POOL_MEAN, lr, 0.0f, static_cast<cudaStream_t>(stream));
+}
+
+emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* momentum,
+                                       const int64_t* indices, const int64_t* offsets,
+                                       int64_t N, int32_t B, const float* per_sample_weights,
+                                       const void* grad_output, emb_pooling mode, float lr,
+                                       float eps, void* stream) {
+  EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
+  if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
+  if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
+  if (p->C != 1) return EMB_ERR_UNSUPPORTED;  // the row-wise norm needs the whole row in one warp
+  if (N == 0) {
+    p->last_kind = 0;
+    return EMB_OK;
+  }
+  if (!momentum || !aligned(momentum, 4)) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
+  return run_sorted(p, 1, vk, weights, momentum, indices, offsets, N, B, per_sample_weights,
+                    grad_output, mode == EMB_POOL_MEAN, lr, eps, static_cast<cudaStream_t>(stream));
+}
+
+emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
+                             const int64_t* offsets, int64_t N, int32_t B,
+                             const void* grad_output, float lr, emb_nobag_path path,
+                             void* stream) {
+  EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
+  if (!p->uniform_D) return EMB_ERR_INVALID_ARG;
+  if (path < EMB_NOBAG_AUTO || path > EMB_NOBAG_ATOMIC) return EMB_ERR_INVALID_ARG;
+  if (path == EMB_NOBAG_ATOMIC && p->wdt != EMB_F32) return EMB_ERR_UNSUPPORTED;
+  if (N == 0) {
+    p->last_kind = 0;
+    return EMB_OK;
+  }
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == EMB_NOBAG_ATOMIC) {
+    const DecodeArgs d = decode_args(p, indices, offsets, nullptr, N, B, 0);
+    EMB_TRY(record(p, 0, s));
+    EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
+    HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N)};
+    EMB_CUDA(launch_hist(ha, p->T, s));
+    for (int i = 1; i <= 4; ++i) EMB_TRY(record(p, i, s));
+    AtomicArgs aa{d, p->ctl, p->sticky, grad_output, static_cast<float*>(weights), p->d_wo,
+                  (uint32_t)p->max_D, lr};
+    EMB_CUDA(launch_nobag_atomic(aa, (int)p->gdt, p->T, s));
+    EMB_TRY(record(p, 5, s));
+    p->last_kind = 2;
+    p->last_N = N;
+    p->last_stream = s;
+    if (p->profiling) p->last_profiled = 2;
+    return EMB_OK;
+  }
+  return run_sorted(p, 0, VK_NOBAG, weights, nullptr, indices, offsets, N, B, nullptr,
+                    grad_output, 0, lr, 0.0f, s);
+}
+
+emb_status emb_plan_status(emb_plan* p) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  if (cudaStreamSynchronize(p->last_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return EMB_ERR_CUDA;
+  }
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, p->sticky, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(p->sticky, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    return EMB_ERR_CUDA;
+  }
+  if (bits & kErrOffsets) return EMB_ERR_INVALID_ARG;  // bag ids (and so tables) are meaningless
+  if (bits & kErrIndex) return EMB_ERR_INDEX_OUT_OF_RANGE;
+  if (bits & kErrTimeout) return EMB_ERR_TIMEOUT;
+  if (bits & kErrCapacity) return EMB_ERR_OOM;
+  return EMB_OK;
+}
+
+emb_status emb_plan_debug_runs(emb_plan* p, int64_t capacity, int64_t* run_keys, int32_t* run_len,
+                               int32_t* cum, int32_t* num_runs, int32_t* long_ids,
+                               int32_t* num_long) {
+  if (!p || capacity < 0) return EMB_ERR_INVALID_ARG;
+  if (p->last_kind == 0) {
+    if (num_runs) *num_runs = 0;
+    if (num_long) *num_long = 0;
+    if (cum && capacity >= 0) cum[0] = 0;
+    return EMB_OK;
+  }
+  if (p->last_kind != 1) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok || cudaStreamSynchronize(p->last_stream) != cudaSuccess) return EMB_ERR_CUDA;
+  Ctl c;
+  if (cudaMemcpy(&c, p->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost) != cudaSuccess) return EMB_ERR_CUDA;
+  if ((int64_t)c.num_runs > capacity || (int64_t)c.num_long > capacity) return EMB_ERR_INVALID_ARG;
+  const uint32_t U = c.num_runs;
+  std::vector<uint32_t> keys(U), starts(U + 1), lids(c.num_long);
+  if (cudaMemcpy(keys.data(), p->run_key, U * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(starts.data(), p->run_start, (U + 1) * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(lids.data(), p->long_ids, c.num_long * sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return EMB_ERR_CUDA;
+  for (uint32_t r = 0; r < U; ++r) {
+    if (run_keys) run_keys[r] = keys[r];
+    if (run_len) run_len[r] = (int32_t)(starts[r + 1] - starts[r]);
+    if (cum) cum[r] = (int32_t)starts[r];
+  }
+  if (cum) cum[U] = (int32_t)starts[U];
+  if (long_ids)
+    for (uint32_t k = 0; k < c.num_long; ++k) long_ids[k] = (int32_t)lids[k];
+  if (num_runs) *num_runs = (int32_t)U;
+  if (num_long) *num_long = (int32_t)c.num_long;
+  return EMB_OK;
+}
+
+emb_status emb_plan_set_profiling(emb_plan* p, int enable) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  if (enable && !p->events_ready) {
+    DeviceGuard g(p->device);
+    for (cudaEvent_t& ev : p->ev)
+      if (cudaEventCreate(&ev) != cudaSuccess) return EMB_ERR_CUDA;
+    p->events_ready = true;
+  }
+  p->profiling = enable != 0;
+  return EMB_OK;
+}
+
+emb_status emb_plan_stage_ms(emb_plan* p, float* ms, int32_t n) {
+  if (!p || !ms || n < 0) return EMB_ERR_INVALID_ARG;
+  if (!p->events_ready || p->last_profiled == 0) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (cudaEventSynchronize(p->ev[kStages]) != cudaSuccess) return EMB_ERR_CUDA;
+  for (int i = 0; i < kStages && i < n; ++i) {
+    float v = 0.f;
+    if (cudaEventElapsedTime(&v, p->ev[i], p->ev[i + 1]) != cudaSuccess) return EMB_ERR_CUDA;
+    ms[i] = v;
+  }
+  return EMB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,359 @@
+// Internal declarations shared by the CUDA translation units of libembbwd.
+//
+// Pipeline of one sorted call (all stream-ordered, no host synchronisation):
+//   memset(ctl) -> k_hist -> k_sort_pass x passes -> k_rle -> k_long -> k_reduce
+//   k_hist      linearises every lookup (hash_size_cumsum[t] + idx), checks it
+//               against its table, validates the CSR offsets and builds the digit
+//               histograms of all radix passes in one read of the indices.
+//   k_sort_pass one LSD radix pass (8-bit digits) with decoupled look-back; the
+//               first pass recomputes the keys from the indices instead of
+//               reading a materialised key array.
+//   k_rle       run-length encode of the sorted keys (unique keys, run starts,
+//               number of runs), one pass with decoupled look-back.
+//   k_long      ordered compaction of runs with >= max_segment_length_per_warp
+//               lookups into block work items (hot rows split into parts).
+//   k_reduce    persistent: block-level work items for long runs (multi-block
+//               parts combined in a fixed order), then one warp per short run;
+//               fp32 accumulation of the scaled gradient rows and the optimizer
+//               update fused in the same kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace embbwd {
+
+constexpr int kThreads = 256;  // every kernel uses 8 warps per block
+constexpr int kWarps = kThreads / 32;
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+constexpr int kMaxPasses = 4;  // 32-bit keys
+constexpr int kRleItems = 8;
+constexpr int kRleTile = kThreads * kRleItems;
+constexpr int kLongItems = 4;
+constexpr int kLongTile = kThreads * kLongItems;
+constexpr int kMaxT = 4096;
+
+// Device-side error bits (per call in Ctl::err, accumulated in the plan's sticky word).
+constexpr uint32_t kErrIndex = 1u;
+constexpr uint32_t kErrOffsets = 2u;
+constexpr uint32_t kErrTimeout = 4u;
+constexpr uint32_t kErrCapacity = 8u;
+
+// Dynamic tile counters, one per kernel of a call.
+enum TileCounter { TC_PASS0 = 0, TC_RLE = kMaxPasses, TC_LONG = kMaxPasses + 1, TC_COUNT = 8 };
+
+// Per-call control block, zeroed by one memset at the start of every call.
+struct Ctl {
+  uint32_t err;
+  uint32_t tile_ctr[TC_COUNT];
+  uint32_t num_runs;
+  uint32_t num_long;
+  uint32_t num_items;
+  uint32_t num_slots;
+  uint32_t item_ctr;
+  uint32_t pad[2];
+  uint32_t hist[kMaxPasses][kRadix];
+};
+
+// Sort-value kinds: what travels with each key through the radix passes.
+enum ValueKind {
+  VK_BAG = 0,         // uint32 bag id t*B+b
+  VK_BAG_SCALED = 1,  // uint64: bag id | float bits of (per-sample weight / L) << 32
+  VK_NOBAG = 2,       // uint32 lookup position l (= gradient row)
+};
+
+// Decoupled look-back status words: [epoch:32 | flag:2 | count:30].
+constexpr uint64_t kFlagAgg = 1ull << 30;
+constexpr uint64_t kFlagInc = 2ull << 30;
+constexpr uint32_t kCountMask = (1u << 30) - 1;
+
+struct LookbackCfg {
+  uint64_t* status;     // [tiles][channels]
+  uint32_t epoch;
+  uint32_t spin_limit;
+  uint32_t force_timeout;  // test flag: give up at once
+};
+
+// What every kernel needs to decode lookups of a tile.
+struct DecodeArgs {
+  const int64_t* indices;
+  const int64_t* offsets;       // [BT+1]
+  const float* psw;             // nullable
+  const uint32_t* hsc;          // [T+1] (device copy of hash_size_cumsum)
+  int64_t N;
+  uint32_t B, T, BT;
+  float invB;
+  int mean;
+};
+
+struct HistArgs {
+  DecodeArgs d;
+  Ctl* ctl;
+  uint32_t* sticky;
+  int passes;
+  int tile;  // lookups per block
+};
+
+struct PassArgs {
+  DecodeArgs d;
+  Ctl* ctl;
+  uint32_t* sticky;
+  LookbackCfg lb;
+  const uint32_t* keys_in;
+  const void* vals_in;
+  uint32_t* keys_out;
+  void* vals_out;
+  int pass;
+  int shift;
+};
+
+struct RleArgs {
+  const uint32_t* keys;  // sorted
+  int64_t N;
+  Ctl* ctl;
+  uint32_t* sticky;
+  LookbackCfg lb;
+  uint32_t* run_key;
+  uint32_t* run_start;  // [U+1]
+};
+
+struct LongArgs {
+  Ctl* ctl;
+  uint32_t* sticky;
+  LookbackCfg lb;
+  const uint32_t* run_start;
+  uint32_t thr;
+  uint32_t part;  // lookups per block work item
+  uint32_t* long_ids;
+  uint32_t* item_base;
+  uint32_t* slot_base;
+  uint32_t* item_long;
+  uint32_t cap_long, cap_items, cap_slots;
+};
+
+struct ReduceArgs {
+  Ctl* ctl;
+  const uint32_t* vals;     // sorted values (uint32 or uint64, per value kind)
+  const uint32_t* run_key;
+  const uint32_t* run_start;
+  const uint32_t* long_ids;
+  const uint32_t* item_base;
+  const uint32_t* slot_base;
+  const uint32_t* item_long;
+  float4* partials;         // [slots * C][KV*32]
+  uint32_t* done;           // [slots * C]
+  const void* grad;
+  void* weights;
+  float* momentum;
+  const uint32_t* hsc;
+  const int32_t* D_offsets;
+  const int64_t* weights_offsets;
+  const int64_t* momentum_offsets;
+  uint32_t T, B;
+  int64_t grad_stride;      // elements per gradient row (sum of D, or D unpooled)
+  float lr, eps;
+  uint32_t thr, part, C;
+};
+
+struct AtomicArgs {
+  DecodeArgs d;
+  Ctl* ctl;
+  uint32_t* sticky;
+  const void* grad;
+  float* weights;
+  const int64_t* weights_offsets;
+  uint32_t D;
+  float lr;
+};
+
+// ---------------------------------------------------------------------------
+// Small device helpers.
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ void raise_error(Ctl* ctl, uint32_t* sticky, uint32_t bits) {
+  atomicOr(&ctl->err, bits);
+  atomicOr(sticky, bits);
+}
+
+// Exclusive scan of one value per thread over a kThreads block. Returns the
+// exclusive prefix; *total gets the block sum. `scratch` holds kWarps words.
+// Contains __syncthreads(); every thread of the block must call it.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();  // scratch may still be read by a previous scan
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  uint32_t wbase = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t s = scratch[w];
+    if (w < warp) wbase += s;
+    tot += s;
+  }
+  *total = tot;
+  return wbase + x - v;
+}
+
+// Decoupled look-back for one channel: publishes this tile's aggregate, walks
+// back over predecessors until an inclusive prefix is found, publishes its own
+// inclusive prefix and returns the exclusive one. Every wait is bounded: after
+// spin_limit polls the tile raises kErrTimeout and carries on with what it has
+// (its successors never wait forever, and nothing is updated in that call).
+__device__ __forceinline__ uint32_t lookback_channel(const LookbackCfg& lb, uint32_t tile,
+                                                     uint32_t channels, uint32_t c, uint32_t agg,
+                                                     Ctl* ctl, uint32_t* sticky) {
+  uint64_t* st = lb.status + (size_t)tile * channels + c;
+  const uint64_t tag = (uint64_t)lb.epoch << 32;
+  if (tile == 0) {
+    st_relaxed_u64(st, tag | kFlagInc | agg);
+    return 0;
+  }
+  st_relaxed_u64(st, tag | kFlagAgg | agg);
+  uint32_t excl = 0;
+  bool failed = lb.force_timeout != 0;
+  int64_t j = (int64_t)tile - 1;
+  while (!failed && j >= 0) {
+    const uint64_t* p = lb.status + (size_t)j * channels + c;
+    uint64_t w = 0;
+    uint32_t spins = 0;
+    for (;;) {
+      w = ld_relaxed_u64(p);
+      if ((uint32_t)(w >> 32) == lb.epoch && (w & (kFlagAgg | kFlagInc))) break;
+      if (++spins > lb.spin_limit) {
+        failed = true;
+        break;
+      }
+      if (spins > 16) __nanosleep(spins > 256 ? 256 : 32);
+    }
+    if (failed) break;
+    excl += (uint32_t)w & kCountMask;
+    if (w & kFlagInc) break;
+    --j;
+  }
+  if (failed) raise_error(ctl, sticky, kErrTimeout);
+  st_relaxed_u64(st, tag | kFlagInc | ((excl + agg) & kCountMask));
+  return excl;
+}
+
+// t = bt / B without an integer divide: a float estimate corrected by one step
+// each way (the estimate is off by at most one for bt < 2^31, T < 2^22).
+__device__ __forceinline__ uint32_t div_by_B(uint32_t bt, uint32_t B, float invB) {
+  uint32_t q = __float2uint_rz((float)bt * invB);
+  if ((uint64_t)q * B > bt) --q;
+  if ((uint64_t)(q + 1) * B <= bt) ++q;
+  return q;
+}
+
+// ---- 4-element vector loads/stores of the storage types, as fp32.
+
+template <typename T>
+struct Vec4;
+
+template <>
+struct Vec4<float> {
+  __device__ __forceinline__ static float4 load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ static float4 load_plain(const float* p) { return *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+};
+
+template <>
+struct Vec4<__half> {
+  __device__ __forceinline__ static float4 cvt(uint2 u) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  __device__ __forceinline__ static float4 load(const __half* p) { return cvt(__ldg(reinterpret_cast<const uint2*>(p))); }
+  __device__ __forceinline__ static float4 load_plain(const __half* p) { return cvt(*reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ static void store(__half* p, float4 v) {
+    const __half2 a = __floats2half2_rn(v.x, v.y);
+    const __half2 b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+template <>
+struct Vec4<__nv_bfloat16> {
+  __device__ __forceinline__ static float4 cvt(uint2 u) {
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  }
+  __device__ __forceinline__ static float4 load(const __nv_bfloat16* p) { return cvt(__ldg(reinterpret_cast<const uint2*>(p))); }
+  __device__ __forceinline__ static float4 load_plain(const __nv_bfloat16* p) { return cvt(*reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ static void store(__nv_bfloat16* p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the .cu files).
+
+struct DevProps {
+  int sms;
+  int smem_optin;
+};
+
+// sort.cu
+size_t sort_tile_for(int64_t N);  // lookups per block for hist and the passes
+cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s);
+cudaError_t launch_sort_pass(const PassArgs& a, int first_kind /* -1: from buffers */,
+                             bool wide_vals, int tile, int T, cudaStream_t s);
+cudaError_t sort_configure(const DevProps& p);
+size_t sort_smem_bytes(int tile, bool wide_vals, bool first, int T);
+
+// runs.cu
+cudaError_t launch_rle(const RleArgs& a, cudaStream_t s);
+cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s);
+
+// reduce_*.cu: one entry per weight type.
+struct ReduceKey {
+  int grad_dtype;   // 0 f32, 1 f16, 2 bf16
+  int optimizer;    // 0 SGD, 1 row-wise Adagrad
+  int value_kind;   // ValueKind
+  int kv;           // 1, 2, 4, 8 vectors of 4 per lane
+};
+// Kernel entry of the requested variant, or nullptr if the combination does not exist.
+const void* reduce_kernel_f32(const ReduceKey& k);
+const void* reduce_kernel_f16(const ReduceKey& k);
+const void* reduce_kernel_bf16(const ReduceKey& k);
+inline size_t reduce_smem_bytes(int kv, int T) {
+  return (size_t)kWarps * kv * 32 * sizeof(float4) + (size_t)(T + 1) * sizeof(uint32_t);
+}
+
+// atomic.cu (the index / offsets check reuses launch_hist with passes = 0)
+cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s);
+cudaError_t atomic_configure();
+
+}  // namespace embbwd

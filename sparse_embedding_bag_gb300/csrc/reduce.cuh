@@ -1,0 +1,354 @@
+// Segment reduce + fused optimizer: for every unique touched row, the sum of
+// the scaled gradient rows of its lookups, accumulated in fp32 registers, then
+// the SGD or row-wise Adagrad update applied once to the row (and its state).
+//
+// Follows the two per-row kernels of
+// "fbgemm_gpu/codegen/embedding_backward_split_template.cu"
+// (*_kernel_warp_per_row_1 for ordinary rows, *_kernel_cta_per_row_1 for rows
+// found by *_find_long_segments) with these changes for sm_103a:
+//   * one persistent kernel instead of two launches: blocks first take block
+//     work items of long runs from a global counter (dynamic, so hot rows are
+//     balanced), then every warp strides over the short runs;
+//   * a very long run is cut into parts of `part` lookups taken by different
+//     blocks; each part writes an fp32 partial row and the last part to arrive
+//     (an atomic counter, no waiting) sums the partials in part order and
+//     applies the optimizer, so the result does not depend on scheduling;
+//   * lanes are grouped by the row width: a row of cvec 16-byte vectors uses
+//     Lg = pow2ceil(cvec) lanes, and 32/Lg lookups are gathered at once;
+//   * the per-lookup scale (per-sample weight / L) travels with the sort
+//     payload, so no gradient copy is made for mean pooling (that page's
+//     grad_mean_kernel writes a scaled copy of grad_output);
+//   * the weight row and its state are read and written exactly once.
+// Optimizer formulas: SGD w -= lr*G; row-wise Adagrad m += sum(G^2)/D,
+// w -= lr*G/(sqrt(m)+eps) ("tt_embeddings_cuda.cu",
+// cache_backward_rowwise_adagrad_approx_kernel), computed in fp32 and rounded
+// once to the weight's storage type.
+#pragma once
+
+#include "internal.cuh"
+
+namespace embbwd {
+
+template <int VK>
+struct ValT {
+  using type = uint32_t;
+};
+template <>
+struct ValT<VK_BAG_SCALED> {
+  using type = uint64_t;
+};
+
+__device__ __forceinline__ uint32_t table_of(const uint32_t* s_hsc, uint32_t T, uint32_t key) {
+  uint32_t lo = 0, hi = T - 1;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi + 1) >> 1;
+    if (s_hsc[mid] <= key) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t log2_pow2ceil32(uint32_t n) {
+  // smallest l with 2^l >= n, capped at 5 (a warp)
+  if (n >= 32) return 5;
+  return n <= 1 ? 0u : 32u - __clz(n - 1);
+}
+
+__device__ __forceinline__ float4 f4_fma(float s, float4 x, float4 acc) {
+  return make_float4(fmaf(s, x.x, acc.x), fmaf(s, x.y, acc.y), fmaf(s, x.z, acc.z), fmaf(s, x.w, acc.w));
+}
+__device__ __forceinline__ float4 f4_add(float4 x, float4 acc) {
+  return make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+}
+
+// Shape of one row task: a chunk of up to KV*32 16-byte vectors of a row.
+struct RowShape {
+  uint32_t t;
+  int64_t idx;
+  uint32_t D;
+  uint32_t cvec_off;  // first vector of the chunk
+  uint32_t cvec;      // vectors in the chunk
+  uint32_t lg;        // log2 of lanes per lookup
+  int64_t goff;       // column offset of the table in a gradient row
+};
+
+template <int VK, typename grad_t, int KV>
+__device__ __forceinline__ void gather_one(const ReduceArgs& a, const RowShape& rs,
+                                           typename ValT<VK>::type v, bool ok, uint32_t li,
+                                           float4 (&acc)[KV]) {
+  const grad_t* grad = static_cast<const grad_t*>(a.grad);
+  const grad_t* row;
+  float scale = 1.0f;
+  if constexpr (VK == VK_NOBAG) {
+    row = grad + (int64_t)(uint32_t)v * a.grad_stride;
+  } else {
+    const uint32_t bt = (uint32_t)v;
+    const uint32_t b = bt - rs.t * a.B;
+    row = grad + (int64_t)b * a.grad_stride + rs.goff;
+    if constexpr (VK == VK_BAG_SCALED) scale = __uint_as_float((uint32_t)(v >> 32));
+  }
+  const uint32_t Lg = 1u << rs.lg;
+  float4 x[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const uint32_t u = li + k * Lg;
+    if (ok && u < rs.cvec) x[k] = Vec4<grad_t>::load(row + (int64_t)(rs.cvec_off + u) * 4);
+    else x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    if constexpr (VK == VK_BAG_SCALED) acc[k] = f4_fma(scale, x[k], acc[k]);
+    else acc[k] = f4_add(x[k], acc[k]);
+  }
+}
+
+// Sum over sorted positions [jb, je) of the run into acc (every lane group ends
+// with the same totals). Lookups are taken 32 at a time; 32/Lg are gathered in
+// parallel, two rounds unrolled for memory-level parallelism.
+template <int VK, typename grad_t, int KV>
+__device__ __forceinline__ void warp_gather_sum(const ReduceArgs& a, const RowShape& rs,
+                                                uint32_t jb, uint32_t je, float4 (&acc)[KV]) {
+  using V = typename ValT<VK>::type;
+  const V* vals = reinterpret_cast<const V*>(a.vals);
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t P = 32u >> rs.lg;
+  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+#pragma unroll
+  for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t j0 = jb; j0 < je; j0 += 32) {
+    const uint32_t n = min(32u, je - j0);
+    const V v = lane < n ? vals[j0 + lane] : (V)0;
+    for (uint32_t s = 0; s < n; s += 2 * P) {
+      const uint32_t s0 = s + g, s1 = s + P + g;
+      const V v0 = __shfl_sync(0xffffffffu, v, s0 & 31);
+      const V v1 = __shfl_sync(0xffffffffu, v, s1 & 31);
+      gather_one<VK, grad_t, KV>(a, rs, v0, s0 < n, li, acc);
+      gather_one<VK, grad_t, KV>(a, rs, v1, s1 < n, li, acc);
+    }
+  }
+#pragma unroll
+  for (uint32_t off = 1u << rs.lg; off < 32; off <<= 1) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      acc[k].x += __shfl_xor_sync(0xffffffffu, acc[k].x, off);
+      acc[k].y += __shfl_xor_sync(0xffffffffu, acc[k].y, off);
+      acc[k].z += __shfl_xor_sync(0xffffffffu, acc[k].z, off);
+      acc[k].w += __shfl_xor_sync(0xffffffffu, acc[k].w, off);
+    }
+  }
+}
+
+template <typename emb_t, int KV>
+__device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs, float4 (&w)[KV]) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+  const emb_t* row = static_cast<const emb_t*>(a.weights) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const uint32_t u = li + (k << rs.lg);
+    if (g == 0 && u < rs.cvec) w[k] = Vec4<emb_t>::load_plain(row + (int64_t)(rs.cvec_off + u) * 4);
+    else w[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Optimizer update of the chunk held by lane group 0 (acc = G, w = old weights).
+template <typename emb_t, int OPT, int KV>
+__device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& rs,
+                                           const float4 (&acc)[KV], const float4 (&w)[KV],
+                                           float m_old) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+  float mult = a.lr;
+  if constexpr (OPT == 1) {
+    float ss = 0.f;
+    if (g == 0) {
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const uint32_t u = li + (k << rs.lg);
+        if (u < rs.cvec) ss += acc[k].x * acc[k].x + acc[k].y * acc[k].y + acc[k].z * acc[k].z + acc[k].w * acc[k].w;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float m_new = m_old + __fdiv_rn(ss, (float)rs.D);
+    mult = __fdiv_rn(a.lr, __fsqrt_rn(m_new) + a.eps);
+    if (lane == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
+  }
+  emb_t* row = static_cast<emb_t*>(a.weights) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const uint32_t u = li + (k << rs.lg);
+    if (g == 0 && u < rs.cvec) {
+      const float4 n = make_float4(fmaf(-mult, acc[k].x, w[k].x), fmaf(-mult, acc[k].y, w[k].y),
+                                   fmaf(-mult, acc[k].z, w[k].z), fmaf(-mult, acc[k].w, w[k].w));
+      Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + u) * 4, n);
+    }
+  }
+}
+
+template <int KV>
+__device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* s_hsc, uint32_t key,
+                                           uint32_t c, RowShape* rs) {
+  rs->t = table_of(s_hsc, a.T, key);
+  rs->idx = (int64_t)(key - s_hsc[rs->t]);
+  const int32_t d0 = __ldg(&a.D_offsets[rs->t]), d1 = __ldg(&a.D_offsets[rs->t + 1]);
+  rs->D = (uint32_t)(d1 - d0);
+  rs->goff = d0;
+  const uint32_t nvec = rs->D >> 2;
+  rs->cvec_off = c * (KV * 32);
+  if (rs->cvec_off >= nvec) return false;
+  rs->cvec = min((uint32_t)(KV * 32), nvec - rs->cvec_off);
+  rs->lg = log2_pow2ceil32(rs->cvec);
+  return true;
+}
+
+template <typename emb_t, typename grad_t, int OPT, int VK, int KV>
+__global__ void __launch_bounds__(kThreads) k_reduce(ReduceArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float4* s_red = reinterpret_cast<float4*>(smem);                       // [8][KV*32]
+  uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_red + kWarps * KV * 32);  // [T+1]
+  __shared__ uint32_t s_item, s_last;
+
+  if (*(volatile uint32_t*)&a.ctl->err) return;  // a check failed earlier in this call
+  for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) s_hsc[i] = a.hsc[i];
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t C = a.C;
+
+  // ---- phase 1: block work items of long runs (dynamic).
+  const uint64_t total_items = (uint64_t)(*(volatile uint32_t*)&a.ctl->num_items) * C;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = atomicAdd(&a.ctl->item_ctr, 1u);
+    __syncthreads();
+    const uint32_t w_all = s_item;
+    if (w_all >= total_items) break;
+    const uint32_t w = C == 1 ? w_all : w_all / C;
+    const uint32_t c = w_all - w * C;
+    const uint32_t kl = a.item_long[w];
+    const uint32_t r = a.long_ids[kl];
+    const uint32_t start = a.run_start[r], end = a.run_start[r + 1];
+    const uint32_t P = (end - start + a.part - 1) / a.part;
+    const uint32_t p = w - a.item_base[kl];
+    const uint32_t ps = start + p * a.part, pe = min(ps + a.part, end);
+    RowShape rs;
+    const bool active = make_shape<KV>(a, s_hsc, a.run_key[r], c, &rs);
+    if (active) {
+      const uint32_t per = (pe - ps + kWarps - 1) / kWarps;
+      const uint32_t wb = min(ps + warp * per, pe), we = min(wb + per, pe);
+      float4 acc[KV];
+      warp_gather_sum<VK, grad_t, KV>(a, rs, wb, we, acc);
+      const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+      if (g == 0) {
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+          const uint32_t u = li + (k << rs.lg);
+          if (u < rs.cvec) s_red[warp * KV * 32 + u] = acc[k];
+        }
+      }
+    }
+    __syncthreads();
+    bool finish = active && P == 1;
+    if (active) {
+      const uint32_t u = threadIdx.x;
+      float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (u < rs.cvec) {
+#pragma unroll
+        for (int wi = 0; wi < kWarps; ++wi) G = f4_add(s_red[wi * KV * 32 + u], G);
+      }
+      if (P == 1) {
+        if (u < rs.cvec) s_red[u] = G;
+      } else {
+        const uint32_t slot0 = a.slot_base[kl];
+        float4* part = a.partials + ((size_t)(slot0 + p) * C + c) * (KV * 32);
+        if (u < rs.cvec) part[u] = G;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          const uint32_t prev = atomicAdd(&a.done[(size_t)slot0 * C + c], 1u);
+          s_last = prev == P - 1;
+        }
+        __syncthreads();
+        if (s_last) {
+          __threadfence();
+          if (u < rs.cvec) {
+            float4 T4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (uint32_t q = 0; q < P; ++q)
+              T4 = f4_add(__ldcg(a.partials + ((size_t)(slot0 + q) * C + c) * (KV * 32) + u), T4);
+            s_red[u] = T4;
+          }
+          if (threadIdx.x == 0) a.done[(size_t)slot0 * C + c] = 0;  // ready for the next call
+          finish = true;
+        }
+      }
+    }
+    __syncthreads();
+    if (finish && warp == 0) {
+      const uint32_t li = lane & ((1u << rs.lg) - 1);
+      float4 acc[KV], wv[KV];
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const uint32_t u = li + (k << rs.lg);
+        acc[k] = u < rs.cvec ? s_red[u] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      load_row<emb_t, KV>(a, rs, wv);
+      float m_old = 0.f;
+      if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+      update_row<emb_t, OPT, KV>(a, rs, acc, wv, m_old);
+    }
+    __syncthreads();
+  }
+
+  // ---- phase 2: one warp per short run (static stride over runs x chunks).
+  const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
+  const uint64_t tasks = (uint64_t)U * C;
+  const uint64_t W = (uint64_t)gridDim.x * kWarps;
+  for (uint64_t task = (uint64_t)blockIdx.x * kWarps + warp; task < tasks; task += W) {
+    const uint32_t r = C == 1 ? (uint32_t)task : (uint32_t)(task / C);
+    const uint32_t c = (uint32_t)(task - (uint64_t)r * C);
+    const uint32_t start = a.run_start[r], end = a.run_start[r + 1];
+    if (end - start >= a.thr) continue;
+    RowShape rs;
+    if (!make_shape<KV>(a, s_hsc, a.run_key[r], c, &rs)) continue;
+    float4 wv[KV];
+    load_row<emb_t, KV>(a, rs, wv);
+    float m_old = 0.f;
+    if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+    float4 acc[KV];
+    warp_gather_sum<VK, grad_t, KV>(a, rs, start, end, acc);
+    update_row<emb_t, OPT, KV>(a, rs, acc, wv, m_old);
+  }
+}
+
+template <typename emb_t, typename grad_t, int OPT, int VK>
+const void* pick_kv(int kv) {
+  switch (kv) {
+    case 1: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 1>);
+    case 2: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 2>);
+    case 4: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 4>);
+    case 8: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 8>);
+    default: return nullptr;
+  }
+}
+
+template <typename emb_t, typename grad_t>
+const void* pick_vk(int opt, int vk, int kv) {
+  if (opt == 0) {
+    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 0, VK_BAG>(kv);
+    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 0, VK_BAG_SCALED>(kv);
+    if (vk == VK_NOBAG) return pick_kv<emb_t, grad_t, 0, VK_NOBAG>(kv);
+  } else if (opt == 1) {
+    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 1, VK_BAG>(kv);
+    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 1, VK_BAG_SCALED>(kv);
+  }
+  return nullptr;
+}
+
+template <typename emb_t>
+const void* pick_reduce(const ReduceKey& k) {
+  switch (k.grad_dtype) {
+    case 0: return pick_vk<emb_t, float>(k.optimizer, k.value_kind, k.kv);
+    case 1: return pick_vk<emb_t, __half>(k.optimizer, k.value_kind, k.kv);
+    case 2: return pick_vk<emb_t, __nv_bfloat16>(k.optimizer, k.value_kind, k.kv);
+    default: return nullptr;
+  }
+}
+
+}  // namespace embbwd

@@ -1,0 +1,284 @@
+// Device radix sort of (linear index, payload) pairs: the sort step of
+// "fbgemm_gpu/codegen/embedding_backward_split_template.cu" (its host function
+// sorts linear_indices with their infos on bits [0, total_hash_size_bits)),
+// written as a one-sweep LSD radix sort for sm_103a:
+//   k_hist       one read of the indices: linearise, range-check, validate the
+//                CSR offsets, and histogram every pass's 8-bit digit;
+//   k_sort_pass  per pass: load a tile, rank it with warp match-based
+//                multisplit, publish/look back per-digit tile counts (decoupled
+//                look-back, bounded waits), scatter through shared memory so
+//                that global writes are runs of consecutive addresses.
+// The first pass rebuilds keys and payloads from the indices, so no key array
+// is ever materialised before sorting. The sort is stable: equal keys keep
+// lookup order.
+#include "decode.cuh"
+
+namespace embbwd {
+
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int ITEMS>
+__global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
+  constexpr int TILE = kThreads * ITEMS;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem);           // [passes][256]
+  uint32_t* s_bag = s_hist + kMaxPasses * kRadix;                  // [TILE]
+  uint32_t* s_hsc = s_bag + TILE;                                  // [T+1]
+  const DecodeArgs& d = a.d;
+  for (int i = threadIdx.x; i < kMaxPasses * kRadix; i += kThreads) s_hist[i] = 0;
+  for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
+
+  // CSR validation: non-decreasing offsets from 0 to N.
+  for (uint32_t bt = blockIdx.x * kThreads + threadIdx.x; bt < d.BT; bt += gridDim.x * kThreads) {
+    if (d.offsets[bt + 1] < d.offsets[bt]) raise_error(a.ctl, a.sticky, kErrOffsets);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (d.offsets[0] != 0 || d.offsets[d.BT] != d.N) raise_error(a.ctl, a.sticky, kErrOffsets);
+  }
+
+  const int64_t i0 = (int64_t)blockIdx.x * TILE;
+  const int64_t i1 = min(i0 + TILE, d.N);
+  __syncthreads();
+  expand_tile_bags(d, i0, i1, s_bag, nullptr);
+
+  bool any_bad = false;
+#pragma unroll
+  for (int k = 0; k < ITEMS; ++k) {
+    const int64_t pos = i0 + k * kThreads + threadIdx.x;
+    const bool valid = pos < i1;
+    uint32_t key = 0;
+    if (valid) {
+      uint32_t t;
+      bool bad;
+      key = linear_key(d, s_hsc, pos, s_bag[pos - i0], &t, &bad);
+      any_bad |= bad;
+    }
+    const uint32_t vmask = __ballot_sync(kFull, valid);
+    for (int p = 0; p < a.passes; ++p) {
+      const uint32_t digit = valid ? ((key >> (p * kRadixBits)) & (kRadix - 1)) : 0xffffffffu;
+      const uint32_t peers = __match_any_sync(kFull, digit);
+      if (valid && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
+        atomicAdd(&s_hist[p * kRadix + digit], (uint32_t)__popc(peers & vmask));
+    }
+  }
+  if (__syncthreads_or(any_bad) && threadIdx.x == 0) raise_error(a.ctl, a.sticky, kErrIndex);
+  for (int i = threadIdx.x; i < a.passes * kRadix; i += kThreads) {
+    const uint32_t c = s_hist[i];
+    if (c) atomicAdd(&a.ctl->hist[0][0] + i, c);
+  }
+}
+
+// FIRST: -1 = keys/values from the previous pass; otherwise the ValueKind the
+// first pass builds from the indices.
+template <int ITEMS, int FIRST, typename V>
+__global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
+  constexpr int TILE = kThreads * ITEMS;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t* s_whist = reinterpret_cast<uint32_t*>(smem);  // [8][256]
+  uint32_t* s_dstart = s_whist + kWarps * kRadix;         // [256]
+  uint32_t* s_gbase = s_dstart + kRadix;                  // [256]
+  uint32_t* s_misc = s_gbase + kRadix;                    // [16]
+  uint32_t* s_keys = s_misc + 16;                         // [TILE]
+  V* s_vals = reinterpret_cast<V*>(s_keys + TILE);        // [TILE]
+  uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_vals + TILE);  // [T+1] (first pass)
+  // The first pass's per-lookup bag ids (and bag lengths) alias the exchange buffers.
+  uint32_t* s_bag = s_keys;
+  uint32_t* s_len = reinterpret_cast<uint32_t*>(s_vals);
+  const DecodeArgs& d = a.d;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
+  for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
+  if constexpr (FIRST >= 0) {
+    for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
+  }
+  __syncthreads();
+  const uint32_t tile = s_misc[0];
+  const int64_t i0 = (int64_t)tile * TILE;
+  const int64_t i1 = min(i0 + TILE, d.N);
+
+  if constexpr (FIRST >= 0)
+    expand_tile_bags(d, i0, i1, s_bag, (FIRST == VK_BAG_SCALED && d.mean) ? s_len : nullptr);
+
+  uint32_t keys[ITEMS];
+  V vals[ITEMS];
+  uint32_t ranks[ITEMS];
+  const int64_t wbase = i0 + (int64_t)warp * 32 * ITEMS;
+#pragma unroll
+  for (int k = 0; k < ITEMS; ++k) {
+    const int64_t pos = wbase + k * 32 + lane;
+    keys[k] = 0;
+    vals[k] = 0;
+    if (pos < i1) {
+      if constexpr (FIRST < 0) {
+        keys[k] = a.keys_in[pos];
+        vals[k] = reinterpret_cast<const V*>(a.vals_in)[pos];
+      } else {
+        const uint32_t bt = s_bag[pos - i0];
+        uint32_t t;
+        bool bad;
+        keys[k] = linear_key(d, s_hsc, pos, bt, &t, &bad);
+        if constexpr (FIRST == VK_BAG) {
+          vals[k] = (V)bt;
+        } else if constexpr (FIRST == VK_NOBAG) {
+          vals[k] = (V)pos;
+        } else {
+          float s = d.psw ? d.psw[pos] : 1.0f;
+          if (d.mean) s = __fdiv_rn(s, (float)s_len[pos - i0]);
+          vals[k] = (V)bt | ((V)__float_as_uint(s) << 32);
+        }
+      }
+    }
+  }
+  if constexpr (FIRST >= 0) __syncthreads();  // s_bag / s_len are dead before the exchange buffers are used
+
+  // Warp-level multisplit ranking: stable within the warp's slice of the tile.
+  const uint32_t lt = lanemask_lt();
+  uint32_t* wh = s_whist + warp * kRadix;
+#pragma unroll
+  for (int k = 0; k < ITEMS; ++k) {
+    const int64_t pos = wbase + k * 32 + lane;
+    const bool valid = pos < i1;
+    const uint32_t digit = valid ? ((keys[k] >> a.shift) & (kRadix - 1)) : kRadix;
+    const uint32_t peers = __match_any_sync(kFull, digit);
+    const int leader = __ffs(peers) - 1;
+    uint32_t pre = 0;
+    if (lane == leader && valid) {
+      pre = wh[digit];
+      wh[digit] = pre + __popc(peers);
+    }
+    pre = __shfl_sync(kFull, pre, leader);
+    ranks[k] = pre + __popc(peers & lt);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // Per digit (one per thread): warp offsets, tile counts, tile and global bases.
+  const uint32_t dg = threadIdx.x;
+  uint32_t count = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t c = s_whist[w * kRadix + dg];
+    s_whist[w * kRadix + dg] = count;
+    count += c;
+  }
+  uint32_t tot;
+  const uint32_t dstart = block_excl_scan(count, s_misc + 8, &tot);
+  const uint32_t gdig = block_excl_scan(a.ctl->hist[a.pass][dg], s_misc + 8, &tot);
+  const uint32_t excl = lookback_channel(a.lb, tile, kRadix, dg, count, a.ctl, a.sticky);
+  s_dstart[dg] = dstart;
+  s_gbase[dg] = gdig + excl - dstart;
+  __syncthreads();
+
+#pragma unroll
+  for (int k = 0; k < ITEMS; ++k) {
+    const int64_t pos = wbase + k * 32 + lane;
+    if (pos < i1) {
+      const uint32_t digit = (keys[k] >> a.shift) & (kRadix - 1);
+      const uint32_t q = s_dstart[digit] + s_whist[warp * kRadix + digit] + ranks[k];
+      s_keys[q] = keys[k];
+      s_vals[q] = vals[k];
+    }
+  }
+  __syncthreads();
+  const uint32_t n = (uint32_t)(i1 - i0);
+  V* vout = reinterpret_cast<V*>(a.vals_out);
+  for (uint32_t q = threadIdx.x; q < n; q += kThreads) {
+    const uint32_t key = s_keys[q];
+    const uint32_t digit = (key >> a.shift) & (kRadix - 1);
+    const uint32_t out = s_gbase[digit] + q;
+    if (out < (uint64_t)d.N) {  // always true unless a look-back timed out
+      a.keys_out[out] = key;
+      vout[out] = s_vals[q];
+    }
+  }
+}
+
+template <int ITEMS>
+size_t hist_smem(int T) {
+  return (kMaxPasses * kRadix + kThreads * ITEMS + T + 1) * sizeof(uint32_t);
+}
+
+template <int ITEMS, typename V>
+size_t pass_smem(int T) {
+  return (kWarps * kRadix + 2 * kRadix + 16) * sizeof(uint32_t) +
+         (size_t)kThreads * ITEMS * (sizeof(uint32_t) + sizeof(V)) + (T + 1) * sizeof(uint32_t);
+}
+
+template <int ITEMS, int FIRST, typename V>
+cudaError_t set_pass_attr(int T) {
+  return cudaFuncSetAttribute(k_sort_pass<ITEMS, FIRST, V>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)pass_smem<ITEMS, V>(T));
+}
+
+template <int ITEMS>
+cudaError_t configure_items(int T) {
+  cudaError_t e = cudaFuncSetAttribute(k_hist<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)hist_smem<ITEMS>(T));
+  if (e == cudaSuccess) e = set_pass_attr<ITEMS, -1, uint32_t>(T);
+  if (e == cudaSuccess) e = set_pass_attr<ITEMS, -1, uint64_t>(T);
+  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_BAG, uint32_t>(T);
+  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_NOBAG, uint32_t>(T);
+  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_BAG_SCALED, uint64_t>(T);
+  return e;
+}
+
+template <int ITEMS, typename V>
+cudaError_t launch_pass_items(const PassArgs& a, int first_kind, int T, cudaStream_t s) {
+  const unsigned grid = (unsigned)((a.d.N + kThreads * ITEMS - 1) / (kThreads * ITEMS));
+  const size_t sm = pass_smem<ITEMS, V>(T);
+  if (first_kind < 0) {
+    k_sort_pass<ITEMS, -1, V><<<grid, kThreads, sm, s>>>(a);
+  } else if (first_kind == VK_BAG_SCALED) {
+    k_sort_pass<ITEMS, VK_BAG_SCALED, uint64_t><<<grid, kThreads, pass_smem<ITEMS, uint64_t>(T), s>>>(a);
+  } else if (first_kind == VK_BAG) {
+    k_sort_pass<ITEMS, VK_BAG, uint32_t><<<grid, kThreads, pass_smem<ITEMS, uint32_t>(T), s>>>(a);
+  } else {
+    k_sort_pass<ITEMS, VK_NOBAG, uint32_t><<<grid, kThreads, pass_smem<ITEMS, uint32_t>(T), s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Lookups per block: small tiles keep all SMs busy on small batches, large
+// tiles cut look-back traffic on large ones.
+size_t sort_tile_for(int64_t N) { return N <= (int64_t)(1 << 21) ? kThreads * 4 : kThreads * 16; }
+
+size_t sort_smem_bytes(int tile, bool wide_vals, bool first, int T) {
+  (void)first;
+  if (tile == kThreads * 4) return wide_vals ? pass_smem<4, uint64_t>(T) : pass_smem<4, uint32_t>(T);
+  return wide_vals ? pass_smem<16, uint64_t>(T) : pass_smem<16, uint32_t>(T);
+}
+
+cudaError_t sort_configure(const DevProps& p) {
+  (void)p;
+  cudaError_t e = configure_items<4>(kMaxT);
+  if (e == cudaSuccess) e = configure_items<16>(kMaxT);
+  return e;
+}
+
+cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s) {
+  const unsigned grid = (unsigned)((a.d.N + a.tile - 1) / a.tile);
+  if (a.tile == kThreads * 4) {
+    k_hist<4><<<grid, kThreads, hist_smem<4>(T), s>>>(a);
+  } else {
+    k_hist<16><<<grid, kThreads, hist_smem<16>(T), s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sort_pass(const PassArgs& a, int first_kind, bool wide_vals, int tile, int T,
+                             cudaStream_t s) {
+  if (tile == kThreads * 4) {
+    return wide_vals ? launch_pass_items<4, uint64_t>(a, first_kind, T, s)
+                     : launch_pass_items<4, uint32_t>(a, first_kind, T, s);
+  }
+  return wide_vals ? launch_pass_items<16, uint64_t>(a, first_kind, T, s)
+                   : launch_pass_items<16, uint32_t>(a, first_kind, T, s);
+}
+
+}  // namespace embbwd

@@ -1,0 +1,183 @@
+"""Thin ctypes binding of libembbwd (include/embbwd.h): same names, argument marshalling only.
+
+Tensors are passed as raw device pointers (``tensor.data_ptr()``); host arrays
+of the plan as numpy buffers. Every computation happens in the CUDA library;
+there is no Python or CPU fallback: if the library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libembbwd.so")
+
+EMB_OK, EMB_ERR_INVALID_ARG, EMB_ERR_UNSUPPORTED, EMB_ERR_INDEX_OUT_OF_RANGE = 0, 1, 2, 3
+EMB_ERR_OOM, EMB_ERR_CUDA, EMB_ERR_TIMEOUT = 4, 5, 6
+EMB_F32, EMB_F16, EMB_BF16 = 0, 1, 2
+EMB_POOL_SUM, EMB_POOL_MEAN = 0, 1
+EMB_NOBAG_AUTO, EMB_NOBAG_SORTED, EMB_NOBAG_ATOMIC = 0, 1, 2
+EMB_FLAG_CHECK_INDICES = 0x1
+EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
+
+# Every symbol include/embbwd.h declares (checked by the tests against the header).
+EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_rowwise_adagrad",
+           "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
+           "emb_plan_stage_ms", "emb_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class EmbError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Loads the library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with sparse_embedding_bag_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, u32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
+        c_int = ctypes.c_int
+        sig = {
+            "emb_bwd_plan": [ctypes.POINTER(vp), c_int, i32, vp, vp, vp, vp, c_int, c_int, i64, i32, i32, u32],
+            "emb_plan_destroy": [vp],
+            "emb_bag_bwd_sgd": [vp, vp, vp, vp, i64, i32, vp, vp, c_int, f32, vp],
+            "emb_bag_bwd_rowwise_adagrad": [vp, vp, vp, vp, vp, i64, i32, vp, vp, c_int, f32, f32, vp],
+            "emb_nobag_bwd_sgd": [vp, vp, vp, vp, i64, i32, vp, f32, c_int, vp],
+            "emb_plan_status": [vp],
+            "emb_plan_debug_runs": [vp, i64, vp, vp, vp, vp, vp, vp],
+            "emb_plan_set_profiling": [vp, c_int],
+            "emb_plan_stage_ms": [vp, vp, i32],
+            "emb_status_string": [c_int],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = c_int
+        lib.emb_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().emb_status_string(int(status)).decode()
+
+
+def _ptr(x):
+    """Device pointer of a tensor, raw int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _host(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st, where):
+    if st != EMB_OK:
+        raise EmbError(st, where)
+    return st
+
+
+def emb_bwd_plan(device, T, hash_size_cumsum, D_offsets, weights_offsets, momentum_offsets,
+                 weight_dtype, grad_dtype, max_N, max_B, max_segment_length_per_warp=0, flags=0):
+    """Returns an opaque plan handle (int). Host arrays are copied by the library."""
+    lib = load()
+    hsc = _host(hash_size_cumsum, np.int64)
+    Do = _host(D_offsets, np.int32)
+    wo = _host(weights_offsets, np.int64)
+    mo = _host(momentum_offsets, np.int64)
+    out = ctypes.c_void_p()
+    st = lib.emb_bwd_plan(ctypes.byref(out), int(device), int(T),
+                          hsc.ctypes.data if hsc is not None else None,
+                          Do.ctypes.data if Do is not None else None,
+                          wo.ctypes.data if wo is not None else None,
+                          mo.ctypes.data if mo is not None else None,
+                          int(weight_dtype), int(grad_dtype), int(max_N), int(max_B),
+                          int(max_segment_length_per_warp), int(flags))
+    _check(st, "emb_bwd_plan")
+    return out.value
+
+
+def emb_plan_destroy(plan):
+    return _check(load().emb_plan_destroy(plan), "emb_plan_destroy")
+
+
+def emb_bag_bwd_sgd(plan, weights, indices, offsets, N, B, per_sample_weights, grad_output, mode,
+                    lr, stream=None):
+    st = load().emb_bag_bwd_sgd(plan, _ptr(weights), _ptr(indices), _ptr(offsets), int(N), int(B),
+                                _ptr(per_sample_weights), _ptr(grad_output), int(mode),
+                                float(lr), _stream(stream))
+    return _check(st, "emb_bag_bwd_sgd")
+
+
+def emb_bag_bwd_rowwise_adagrad(plan, weights, momentum, indices, offsets, N, B,
+                                per_sample_weights, grad_output, mode, lr, eps, stream=None):
+    st = load().emb_bag_bwd_rowwise_adagrad(plan, _ptr(weights), _ptr(momentum), _ptr(indices),
+                                            _ptr(offsets), int(N), int(B),
+                                            _ptr(per_sample_weights), _ptr(grad_output),
+                                            int(mode), float(lr), float(eps), _stream(stream))
+    return _check(st, "emb_bag_bwd_rowwise_adagrad")
+
+
+def emb_nobag_bwd_sgd(plan, weights, indices, offsets, N, B, grad_output, lr,
+                      path=EMB_NOBAG_AUTO, stream=None):
+    st = load().emb_nobag_bwd_sgd(plan, _ptr(weights), _ptr(indices), _ptr(offsets), int(N),
+                                  int(B), _ptr(grad_output), float(lr), int(path), _stream(stream))
+    return _check(st, "emb_nobag_bwd_sgd")
+
+
+def emb_plan_status(plan):
+    """Returns the latched device status code (does not raise)."""
+    return load().emb_plan_status(plan)
+
+
+def emb_plan_debug_runs(plan, capacity):
+    """Integer outputs of the last sorted call as numpy arrays."""
+    cap = int(capacity)
+    run_keys = np.zeros(max(cap, 1), np.int64)
+    run_len = np.zeros(max(cap, 1), np.int32)
+    cum = np.zeros(cap + 1, np.int32)
+    long_ids = np.zeros(max(cap, 1), np.int32)
+    nr = ctypes.c_int32(0)
+    nl = ctypes.c_int32(0)
+    st = load().emb_plan_debug_runs(plan, cap, run_keys.ctypes.data, run_len.ctypes.data,
+                                    cum.ctypes.data, ctypes.addressof(nr), long_ids.ctypes.data,
+                                    ctypes.addressof(nl))
+    _check(st, "emb_plan_debug_runs")
+    u, l = nr.value, nl.value
+    return {"run_keys": run_keys[:u], "run_len": run_len[:u], "cum": cum[:u + 1],
+            "num_runs": u, "long_ids": long_ids[:l]}
+
+
+def emb_plan_set_profiling(plan, enable):
+    return _check(load().emb_plan_set_profiling(plan, int(bool(enable))), "emb_plan_set_profiling")
+
+
+def emb_plan_stage_ms(plan, n=5):
+    out = np.zeros(n, np.float32)
+    _check(load().emb_plan_stage_ms(plan, out.ctypes.data, n), "emb_plan_stage_ms")
+    return out
