@@ -69,6 +69,9 @@ typedef enum { EMB_NOBAG_AUTO = 0, EMB_NOBAG_SORTED = 1, EMB_NOBAG_ATOMIC = 2 } 
 
 /* emb_bwd_plan flags. Index range checking is always on. */
 #define EMB_FLAG_CHECK_INDICES 0x1u
+/* Launch the kernels of a call as plain stream-ordered launches instead of
+ * programmatic dependent launches (for A/B timing; results are identical). */
+#define EMB_FLAG_NO_PDL 0x2u
 /* Test only: every block that would wait on another one gives up at once and
  * reports EMB_ERR_TIMEOUT, exercising the error path without a real stall. */
 #define EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u

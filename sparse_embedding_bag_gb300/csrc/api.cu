@@ -164,11 +164,12 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
   const bool wide = vk == VK_BAG_SCALED;
   const LookbackCfg lb0{p->status, epoch, kSpinLimit, (p->flags & EMB_FLAG_DEBUG_FORCE_TIMEOUT) ? 1u : 0u};
+  const bool pdl = !(p->flags & EMB_FLAG_NO_PDL);
 
   EMB_TRY(record(p, 0, s));
   EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
   HistArgs ha{d, p->ctl, p->sticky, passes, tile};
-  EMB_CUDA(launch_hist(ha, p->T, s));
+  EMB_CUDA(launch_hist(ha, p->T, s, pdl));
   EMB_TRY(record(p, 1, s));
   for (int pass = 0; pass < passes; ++pass) {
     PassArgs pa;
@@ -184,13 +185,13 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_out = p->vals[out];
     pa.pass = pass;
     pa.shift = pass * kRadixBits;
-    EMB_CUDA(launch_sort_pass(pa, pass == 0 ? vk : -1, wide, tile, p->T, s));
+    EMB_CUDA(launch_sort_pass(pa, pass == 0 ? vk : -1, wide, tile, p->T, s, pdl));
   }
   const int fin = (passes - 1) & 1;
   EMB_TRY(record(p, 2, s));
   RleArgs ra{p->keys[fin], N, p->ctl, p->sticky, lb0, p->run_key, p->run_start};
   ra.lb.epoch = epoch + 5;
-  EMB_CUDA(launch_rle(ra, s));
+  EMB_CUDA(launch_rle(ra, s, pdl));
   EMB_TRY(record(p, 3, s));
   LongArgs la;
   la.ctl = p->ctl;
@@ -209,7 +210,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   la.cap_slots = p->cap_slots;
   const int64_t long_tiles = (N + kLongTile - 1) / kLongTile;
   const int long_grid = (int)std::min<int64_t>(long_tiles, 2 * (int64_t)p->props.sms);
-  EMB_CUDA(launch_long(la, long_grid, s));
+  EMB_CUDA(launch_long(la, long_grid, s, pdl));
   EMB_TRY(record(p, 4, s));
 
   ReduceArgs r;
@@ -241,8 +242,8 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
-  EMB_CUDA(cudaLaunchKernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads), args,
-                            reduce_smem_bytes(p->kv, p->T), s));
+  EMB_CUDA(launch_kernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads),
+                         reduce_smem_bytes(p->kv, p->T), s, args, pdl));
   EMB_TRY(record(p, 5, s));
   p->last_kind = 1;
   p->last_N = N;
@@ -479,15 +480,16 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
   if (!g.ok) return EMB_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == EMB_NOBAG_ATOMIC) {
+    const bool pdl = !(p->flags & EMB_FLAG_NO_PDL);
     const DecodeArgs d = decode_args(p, indices, offsets, nullptr, N, B, 0);
     EMB_TRY(record(p, 0, s));
     EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
     HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N)};
-    EMB_CUDA(launch_hist(ha, p->T, s));
+    EMB_CUDA(launch_hist(ha, p->T, s, pdl));
     for (int i = 1; i <= 4; ++i) EMB_TRY(record(p, i, s));
     AtomicArgs aa{d, p->ctl, p->sticky, grad_output, static_cast<float*>(weights), p->d_wo,
                   (uint32_t)p->max_D, lr};
-    EMB_CUDA(launch_nobag_atomic(aa, (int)p->gdt, p->T, s));
+    EMB_CUDA(launch_nobag_atomic(aa, (int)p->gdt, p->T, s, pdl));
     EMB_TRY(record(p, 5, s));
     p->last_kind = 2;
     p->last_N = N;

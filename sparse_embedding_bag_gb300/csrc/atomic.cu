@@ -19,6 +19,8 @@ constexpr int kAtomicTile = 64;  // lookups per block
 template <typename grad_t>
 __global__ void __launch_bounds__(kThreads) k_nobag_atomic(AtomicArgs a) {
   __shared__ uint32_t s_bag[kAtomicTile];
+  pdl_wait();
+  pdl_trigger();
   if (*(volatile uint32_t*)&a.ctl->err) return;
   const DecodeArgs& d = a.d;
   const int64_t i0 = (int64_t)blockIdx.x * kAtomicTile;
@@ -48,15 +50,15 @@ __global__ void __launch_bounds__(kThreads) k_nobag_atomic(AtomicArgs a) {
 
 cudaError_t atomic_configure() { return cudaSuccess; }
 
-cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s) {
+cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s, bool pdl) {
   (void)T;
   const unsigned grid = (unsigned)((a.d.N + kAtomicTile - 1) / kAtomicTile);
-  switch (grad_dtype) {
-    case 0: k_nobag_atomic<float><<<grid, kThreads, 0, s>>>(a); break;
-    case 1: k_nobag_atomic<__half><<<grid, kThreads, 0, s>>>(a); break;
-    default: k_nobag_atomic<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a); break;
-  }
-  return cudaGetLastError();
+  AtomicArgs arg = a;
+  void* args[] = {&arg};
+  const void* fn = grad_dtype == 0   ? reinterpret_cast<const void*>(&k_nobag_atomic<float>)
+                   : grad_dtype == 1 ? reinterpret_cast<const void*>(&k_nobag_atomic<__half>)
+                                     : reinterpret_cast<const void*>(&k_nobag_atomic<__nv_bfloat16>);
+  return launch_kernel(fn, dim3(grid), dim3(kThreads), 0, s, args, pdl);
 }
 
 }  // namespace embbwd

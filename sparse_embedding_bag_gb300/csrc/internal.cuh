@@ -182,6 +182,14 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Programmatic dependent launch: every kernel of a call is launched so that
+// it may start while its predecessor drains. pdl_wait() blocks until the
+// predecessor grid has completed and its writes are visible (a no-op when the
+// kernel was launched without the attribute); pdl_trigger() lets the next
+// kernel start launching once every block of this grid has reached it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -325,17 +333,34 @@ struct DevProps {
   int smem_optin;
 };
 
+// Launches fn(*args[0]) on `s`; with pdl set, as a programmatic dependent of
+// the previous kernel on the stream (see pdl_wait / pdl_trigger).
+inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 void** args, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // sort.cu
 size_t sort_tile_for(int64_t N);  // lookups per block for hist and the passes
-cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s);
+cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s, bool pdl);
 cudaError_t launch_sort_pass(const PassArgs& a, int first_kind /* -1: from buffers */,
-                             bool wide_vals, int tile, int T, cudaStream_t s);
+                             bool wide_vals, int tile, int T, cudaStream_t s, bool pdl);
 cudaError_t sort_configure(const DevProps& p);
 size_t sort_smem_bytes(int tile, bool wide_vals, bool first, int T);
 
 // runs.cu
-cudaError_t launch_rle(const RleArgs& a, cudaStream_t s);
-cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_rle(const RleArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s, bool pdl);
 
 // reduce_*.cu: one entry per weight type.
 struct ReduceKey {
@@ -353,7 +378,7 @@ inline size_t reduce_smem_bytes(int kv, int T) {
 }
 
 // atomic.cu (the index / offsets check reuses launch_hist with passes = 0)
-cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s);
+cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s, bool pdl);
 cudaError_t atomic_configure();
 
 }  // namespace embbwd

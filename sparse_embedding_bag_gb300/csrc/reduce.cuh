@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce(ReduceArgs a) {
   uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_red + kWarps * KV * 32);  // [T+1]
   __shared__ uint32_t s_item, s_last;
 
+  pdl_wait();
+  pdl_trigger();
   if (*(volatile uint32_t*)&a.ctl->err) return;  // a check failed earlier in this call
   for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) s_hsc[i] = a.hsc[i];
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

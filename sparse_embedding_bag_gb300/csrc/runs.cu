@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kThreads) k_rle(RleArgs a) {
   __shared__ uint32_t s_tile;
   __shared__ uint32_t s_scan[kWarps];
   __shared__ uint32_t s_base;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
   __syncthreads();
   const uint32_t tile = s_tile;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(kThreads) k_long(LongArgs a) {
   __shared__ uint32_t s_tile;
   __shared__ uint32_t s_scan[kWarps];
   __shared__ uint32_t s_base[3];
+  pdl_wait();
+  pdl_trigger();
   const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
   for (;;) {
     if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_LONG], 1u);
@@ -142,15 +146,17 @@ __global__ void __launch_bounds__(kThreads) k_long(LongArgs a) {
 
 }  // namespace
 
-cudaError_t launch_rle(const RleArgs& a, cudaStream_t s) {
+cudaError_t launch_rle(const RleArgs& a, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.N + kRleTile - 1) / kRleTile);
-  k_rle<<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  RleArgs arg = a;
+  void* args[] = {&arg};
+  return launch_kernel(reinterpret_cast<const void*>(&k_rle), dim3(grid), dim3(kThreads), 0, s, args, pdl);
 }
 
-cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s) {
-  k_long<<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s, bool pdl) {
+  LongArgs arg = a;
+  void* args[] = {&arg};
+  return launch_kernel(reinterpret_cast<const void*>(&k_long), dim3(grid), dim3(kThreads), 0, s, args, pdl);
 }
 
 }  // namespace embbwd

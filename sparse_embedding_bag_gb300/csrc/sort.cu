@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
   uint32_t* s_bag = s_hist + kMaxPasses * kRadix;                  // [TILE]
   uint32_t* s_hsc = s_bag + TILE;                                  // [T+1]
   const DecodeArgs& d = a.d;
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < kMaxPasses * kRadix; i += kThreads) s_hist[i] = 0;
   for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
 
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
   uint32_t* s_len = reinterpret_cast<uint32_t*>(s_vals);
   const DecodeArgs& d = a.d;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
 
   if (threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
   for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
@@ -227,19 +231,26 @@ cudaError_t configure_items(int T) {
 }
 
 template <int ITEMS, typename V>
-cudaError_t launch_pass_items(const PassArgs& a, int first_kind, int T, cudaStream_t s) {
+cudaError_t launch_pass_items(const PassArgs& a, int first_kind, int T, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.d.N + kThreads * ITEMS - 1) / (kThreads * ITEMS));
-  const size_t sm = pass_smem<ITEMS, V>(T);
+  PassArgs arg = a;
+  void* args[] = {&arg};
+  const void* fn;
+  size_t sm;
   if (first_kind < 0) {
-    k_sort_pass<ITEMS, -1, V><<<grid, kThreads, sm, s>>>(a);
+    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, -1, V>);
+    sm = pass_smem<ITEMS, V>(T);
   } else if (first_kind == VK_BAG_SCALED) {
-    k_sort_pass<ITEMS, VK_BAG_SCALED, uint64_t><<<grid, kThreads, pass_smem<ITEMS, uint64_t>(T), s>>>(a);
+    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_BAG_SCALED, uint64_t>);
+    sm = pass_smem<ITEMS, uint64_t>(T);
   } else if (first_kind == VK_BAG) {
-    k_sort_pass<ITEMS, VK_BAG, uint32_t><<<grid, kThreads, pass_smem<ITEMS, uint32_t>(T), s>>>(a);
+    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_BAG, uint32_t>);
+    sm = pass_smem<ITEMS, uint32_t>(T);
   } else {
-    k_sort_pass<ITEMS, VK_NOBAG, uint32_t><<<grid, kThreads, pass_smem<ITEMS, uint32_t>(T), s>>>(a);
+    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_NOBAG, uint32_t>);
+    sm = pass_smem<ITEMS, uint32_t>(T);
   }
-  return cudaGetLastError();
+  return launch_kernel(fn, dim3(grid), dim3(kThreads), sm, s, args, pdl);
 }
 
 }  // namespace
@@ -261,24 +272,25 @@ cudaError_t sort_configure(const DevProps& p) {
   return e;
 }
 
-cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s) {
+cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.d.N + a.tile - 1) / a.tile);
-  if (a.tile == kThreads * 4) {
-    k_hist<4><<<grid, kThreads, hist_smem<4>(T), s>>>(a);
-  } else {
-    k_hist<16><<<grid, kThreads, hist_smem<16>(T), s>>>(a);
-  }
-  return cudaGetLastError();
+  HistArgs arg = a;
+  void* args[] = {&arg};
+  if (a.tile == kThreads * 4)
+    return launch_kernel(reinterpret_cast<const void*>(&k_hist<4>), dim3(grid), dim3(kThreads),
+                         hist_smem<4>(T), s, args, pdl);
+  return launch_kernel(reinterpret_cast<const void*>(&k_hist<16>), dim3(grid), dim3(kThreads),
+                       hist_smem<16>(T), s, args, pdl);
 }
 
 cudaError_t launch_sort_pass(const PassArgs& a, int first_kind, bool wide_vals, int tile, int T,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool pdl) {
   if (tile == kThreads * 4) {
-    return wide_vals ? launch_pass_items<4, uint64_t>(a, first_kind, T, s)
-                     : launch_pass_items<4, uint32_t>(a, first_kind, T, s);
+    return wide_vals ? launch_pass_items<4, uint64_t>(a, first_kind, T, s, pdl)
+                     : launch_pass_items<4, uint32_t>(a, first_kind, T, s, pdl);
   }
-  return wide_vals ? launch_pass_items<16, uint64_t>(a, first_kind, T, s)
-                   : launch_pass_items<16, uint32_t>(a, first_kind, T, s);
+  return wide_vals ? launch_pass_items<16, uint64_t>(a, first_kind, T, s, pdl)
+                   : launch_pass_items<16, uint32_t>(a, first_kind, T, s, pdl);
 }
 
 }  // namespace embbwd

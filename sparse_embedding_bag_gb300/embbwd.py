@@ -21,6 +21,7 @@ EMB_F32, EMB_F16, EMB_BF16 = 0, 1, 2
 EMB_POOL_SUM, EMB_POOL_MEAN = 0, 1
 EMB_NOBAG_AUTO, EMB_NOBAG_SORTED, EMB_NOBAG_ATOMIC = 0, 1, 2
 EMB_FLAG_CHECK_INDICES = 0x1
+EMB_FLAG_NO_PDL = 0x2
 EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 
 # Every symbol include/embbwd.h declares (checked by the tests against the header).
