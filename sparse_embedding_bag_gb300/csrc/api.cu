@@ -18,7 +18,8 @@ using namespace embbwd;
 namespace {
 
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls before a look-back wait gives up (~1 s)
-constexpr uint32_t kPart = 1024;           // lookups per block work item of a long run
+constexpr uint32_t kMaxPart = 1024;        // lookups per block work item of a long run, at most
+constexpr uint32_t kMinPart = 32;
 constexpr int kStages = 5;
 
 struct DeviceGuard {
@@ -35,6 +36,12 @@ struct DeviceGuard {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+uint32_t pow2floor(uint64_t x) {
+  uint32_t r = 1;
+  while ((uint64_t)r * 2 <= x && r < (1u << 30)) r *= 2;
+  return r;
+}
+
 }  // namespace
 
 struct emb_plan {
@@ -50,6 +57,8 @@ struct emb_plan {
   int kv = 1;
   uint32_t C = 1;
   int key_bits = 1;
+  uint32_t team_log2 = 5;
+  uint32_t base_part = kMaxPart;
   std::vector<uint32_t> hsc;
   std::vector<int32_t> Do;
   DevProps props{};
@@ -64,6 +73,7 @@ struct emb_plan {
   uint32_t* keys[2] = {nullptr, nullptr};
   void* vals[2] = {nullptr, nullptr};
   uint64_t* status = nullptr;
+  uint32_t* tile_bags = nullptr;
   uint32_t* run_key = nullptr;
   uint32_t* run_start = nullptr;
   uint32_t* long_ids = nullptr;
@@ -105,6 +115,14 @@ emb_status record(emb_plan* p, int i, cudaStream_t s) {
                             ? cudaEventRecordWithFlags(p->ev[i], s, cudaEventRecordExternal)
                             : cudaEventRecord(p->ev[i], s);
   return e == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
+}
+
+// Lookups per block work item of a long run: about 64 KB of gradient reads
+// (base_part), raised for large batches so that there are a few items per
+// resident warp rather than many tiny ones.
+uint32_t part_for(const emb_plan* p, int64_t N) {
+  const uint32_t by_n = pow2floor((uint64_t)N / (32ull * p->props.sms));
+  return std::min(kMaxPart, std::max(p->base_part, by_n));
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -168,7 +186,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
 
   EMB_TRY(record(p, 0, s));
   EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
-  HistArgs ha{d, p->ctl, p->sticky, passes, tile};
+  HistArgs ha{d, p->ctl, p->sticky, passes, tile, p->tile_bags};
   EMB_CUDA(launch_hist(ha, p->T, s, pdl));
   EMB_TRY(record(p, 1, s));
   for (int pass = 0; pass < passes; ++pass) {
@@ -178,6 +196,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.sticky = p->sticky;
     pa.lb = lb0;
     pa.lb.epoch = epoch + (uint32_t)pass;
+    pa.tile_bags = p->tile_bags;
     const int in = (pass + 1) & 1, out = pass & 1;
     pa.keys_in = p->keys[in];
     pa.vals_in = p->vals[in];
@@ -200,7 +219,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   la.lb.epoch = epoch + 6;
   la.run_start = p->run_start;
   la.thr = p->thr;
-  la.part = kPart;
+  la.part = part_for(p, N);
   la.long_ids = p->long_ids;
   la.item_base = p->item_base;
   la.slot_base = p->slot_base;
@@ -237,8 +256,9 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.lr = lr;
   r.eps = eps;
   r.thr = p->thr;
-  r.part = kPart;
+  r.part = la.part;
   r.C = p->C;
+  r.team_log2 = p->team_log2;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
@@ -312,6 +332,12 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   const int nvec = max_D / 4;
   p->kv = nvec <= 32 ? 1 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
   p->C = (uint32_t)((nvec + p->kv * 32 - 1) / (p->kv * 32));
+  // Short runs: teams of lanes as wide as the widest row (in 16-byte vectors, at most a warp).
+  p->team_log2 = 0;
+  while ((1 << p->team_log2) < std::min(nvec, 32)) ++p->team_log2;
+  // Long runs: parts of about 64 KB of gradient reads (one row chunk per lookup).
+  const uint32_t chunk_bytes = (uint32_t)std::min(max_D, p->kv * 128) * (grad_dtype == EMB_F32 ? 4u : 2u);
+  p->base_part = std::min(kMaxPart, std::max(kMinPart, pow2floor(65536 / chunk_bytes)));
   const uint64_t total_rows = (uint64_t)hash_size_cumsum[T];
   p->key_bits = 1;
   while (p->key_bits < 32 && ((uint64_t)1 << p->key_bits) < total_rows) ++p->key_bits;
@@ -337,9 +363,12 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   const uint64_t sort_tiles = std::max<uint64_t>((N + 1023) / 1024, 1);  // smallest tile is 1024
   const uint64_t status_words = std::max<uint64_t>(
       sort_tiles * kRadix, std::max<uint64_t>((N + kRleTile - 1) / kRleTile, (N + kLongTile - 1) / kLongTile * 3));
+  // part_for(N) >= N / (2 * sms * 32) and >= base_part, so no call has more than
+  // max(N / kMaxPart, 2 * sms * 32) long-run parts beyond one per long run.
+  const uint64_t parts_bound = std::max<uint64_t>(N / kMaxPart + 1, 2ull * p->props.sms * 32 + 1);
   p->cap_long = (uint32_t)(N / p->thr + 1);
-  p->cap_items = (uint32_t)(N / kPart + p->cap_long + 1);
-  p->cap_slots = (uint32_t)(2 * (N / kPart) + 2);
+  p->cap_items = (uint32_t)std::min<uint64_t>(parts_bound + p->cap_long, N + 1);
+  p->cap_slots = (uint32_t)(2 * parts_bound + 2);
   const size_t part_row = (size_t)p->kv * 32 * sizeof(float4);
   struct Seg {
     void** ptr;
@@ -359,6 +388,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {&p->vals[0], N * sizeof(uint64_t)},
       {&p->vals[1], N * sizeof(uint64_t)},
       {reinterpret_cast<void**>(&p->status), status_words * sizeof(uint64_t)},
+      {reinterpret_cast<void**>(&p->tile_bags), 2 * sort_tiles * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->run_key), N * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
@@ -484,7 +514,7 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
     const DecodeArgs d = decode_args(p, indices, offsets, nullptr, N, B, 0);
     EMB_TRY(record(p, 0, s));
     EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
-    HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N)};
+    HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N), p->tile_bags};
     EMB_CUDA(launch_hist(ha, p->T, s, pdl));
     for (int i = 1; i <= 4; ++i) EMB_TRY(record(p, i, s));
     AtomicArgs aa{d, p->ctl, p->sticky, grad_output, static_cast<float*>(weights), p->d_wo,

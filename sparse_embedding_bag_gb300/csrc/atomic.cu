@@ -19,13 +19,14 @@ constexpr int kAtomicTile = 64;  // lookups per block
 template <typename grad_t>
 __global__ void __launch_bounds__(kThreads) k_nobag_atomic(AtomicArgs a) {
   __shared__ uint32_t s_bag[kAtomicTile];
+  __shared__ int64_t s_off[2 * kAtomicTile];
   pdl_wait();
   pdl_trigger();
   if (*(volatile uint32_t*)&a.ctl->err) return;
   const DecodeArgs& d = a.d;
   const int64_t i0 = (int64_t)blockIdx.x * kAtomicTile;
   const int64_t i1 = min(i0 + kAtomicTile, d.N);
-  if (d.T > 1) expand_tile_bags(d, i0, i1, s_bag, nullptr);
+  if (d.T > 1) expand_tile_bags(d, i0, i1, s_bag, nullptr, s_off, 2 * kAtomicTile);
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t nvec = a.D >> 2;
   const grad_t* grad = static_cast<const grad_t*>(a.grad);

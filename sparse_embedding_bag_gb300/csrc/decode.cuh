@@ -45,16 +45,28 @@ __device__ __forceinline__ void block_bag_search2(const int64_t* __restrict__ of
   *r1 = lo1;
 }
 
-// Fills s_bag[i - i0] with the bag id of every lookup i in [i0, i1) and, when
-// s_len is not null, s_len[i - i0] with that bag's length. Contains barriers.
-__device__ __forceinline__ void expand_tile_bags(const DecodeArgs& d, int64_t i0, int64_t i1,
-                                                 uint32_t* s_bag, uint32_t* s_len) {
-  uint32_t bt_lo, bt_hi;
-  block_bag_search2(d.offsets, d.BT, i0, i1 - 1, &bt_lo, &bt_hi);
-  if (bt_hi < bt_lo) bt_hi = bt_lo;
+// Fills s_bag[i - i0] with the bag id of every lookup i in [i0, i1) from the
+// bags [bt_lo, bt_hi] that overlap the tile and, when s_len is not null,
+// s_len[i - i0] with that bag's length. Ends with a barrier.
+// The offsets of the overlapping bags are first staged in shared memory
+// (s_off, room for off_cap entries) with one parallel load, so that the per-bag
+// loop does not wait on a global load per bag; a window that does not fit is
+// read from global memory directly.
+__device__ __forceinline__ void expand_bag_range(const DecodeArgs& d, int64_t i0, int64_t i1,
+                                                 uint32_t bt_lo, uint32_t bt_hi, uint32_t* s_bag,
+                                                 uint32_t* s_len, int64_t* s_off, uint32_t off_cap) {
+  if (bt_hi >= d.BT) bt_hi = d.BT - 1;
+  if (bt_lo > bt_hi) bt_lo = bt_hi;
+  const uint32_t span = bt_hi - bt_lo + 1;
+  const bool staged = span + 1 <= off_cap;
+  if (staged) {
+    for (uint32_t k = threadIdx.x; k <= span; k += kThreads) s_off[k] = d.offsets[bt_lo + k];
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (uint32_t bt = bt_lo + warp; bt <= bt_hi; bt += kWarps) {
-    const int64_t a = d.offsets[bt], e = d.offsets[bt + 1];
+    const int64_t a = staged ? s_off[bt - bt_lo] : d.offsets[bt];
+    const int64_t e = staged ? s_off[bt - bt_lo + 1] : d.offsets[bt + 1];
     const int64_t lo = a > i0 ? a : i0;
     const int64_t hi = e < i1 ? e : i1;
     const uint32_t L = (uint32_t)(e - a);
@@ -64,6 +76,19 @@ __device__ __forceinline__ void expand_tile_bags(const DecodeArgs& d, int64_t i0
     }
   }
   __syncthreads();
+}
+
+// Same, finding the overlapping bags first. Contains barriers; returns the range.
+__device__ __forceinline__ void expand_tile_bags(const DecodeArgs& d, int64_t i0, int64_t i1,
+                                                 uint32_t* s_bag, uint32_t* s_len, int64_t* s_off,
+                                                 uint32_t off_cap, uint32_t* lo_out = nullptr,
+                                                 uint32_t* hi_out = nullptr) {
+  uint32_t bt_lo, bt_hi;
+  block_bag_search2(d.offsets, d.BT, i0, i1 - 1, &bt_lo, &bt_hi);
+  if (bt_hi < bt_lo) bt_hi = bt_lo;
+  if (lo_out) *lo_out = bt_lo;
+  if (hi_out) *hi_out = bt_hi;
+  expand_bag_range(d, i0, i1, bt_lo, bt_hi, s_bag, s_len, s_off, off_cap);
 }
 
 // Linear index (32-bit) of lookup `pos` whose bag is `bt`; sets *bad when the

@@ -94,7 +94,8 @@ struct HistArgs {
   Ctl* ctl;
   uint32_t* sticky;
   int passes;
-  int tile;  // lookups per block
+  int tile;              // lookups per block
+  uint32_t* tile_bags;   // out: [2 * tiles] first and last bag overlapping each tile
 };
 
 struct PassArgs {
@@ -102,6 +103,7 @@ struct PassArgs {
   Ctl* ctl;
   uint32_t* sticky;
   LookbackCfg lb;
+  const uint32_t* tile_bags;  // from k_hist (same tile size), used by the first pass
   const uint32_t* keys_in;
   const void* vals_in;
   uint32_t* keys_out;
@@ -156,6 +158,7 @@ struct ReduceArgs {
   int64_t grad_stride;      // elements per gradient row (sum of D, or D unpooled)
   float lr, eps;
   uint32_t thr, part, C;
+  uint32_t team_log2;       // lanes per team of the short-run phase: 2^team_log2
 };
 
 struct AtomicArgs {
@@ -241,29 +244,91 @@ __device__ __forceinline__ uint32_t lookback_channel(const LookbackCfg& lb, uint
     return 0;
   }
   st_relaxed_u64(st, tag | kFlagAgg | agg);
+  // Windowed walk: kLookbackWindow predecessors are read per poll (independent
+  // loads in flight), so a chain of tiles that published only aggregates is
+  // crossed kLookbackWindow tiles per memory round trip.
+  constexpr int kWin = 16;
   uint32_t excl = 0;
   bool failed = lb.force_timeout != 0;
   int64_t j = (int64_t)tile - 1;
+  uint32_t polls = 0;
   while (!failed && j >= 0) {
-    const uint64_t* p = lb.status + (size_t)j * channels + c;
-    uint64_t w = 0;
-    uint32_t spins = 0;
-    for (;;) {
-      w = ld_relaxed_u64(p);
-      if ((uint32_t)(w >> 32) == lb.epoch && (w & (kFlagAgg | kFlagInc))) break;
-      if (++spins > lb.spin_limit) {
+    uint64_t w[kWin];
+#pragma unroll
+    for (int k = 0; k < kWin; ++k)
+      w[k] = j - k >= 0 ? ld_relaxed_u64(lb.status + (size_t)(j - k) * channels + c) : (tag | kFlagInc);
+    int k = 0;
+    bool done = false;
+#pragma unroll
+    for (int q = 0; q < kWin; ++q) {
+      if (k != q) continue;  // an earlier word was not ready
+      const uint64_t x = w[q];
+      if ((uint32_t)(x >> 32) != lb.epoch || !(x & (kFlagAgg | kFlagInc))) continue;
+      excl += (uint32_t)x & kCountMask;
+      if (x & kFlagInc) {
+        done = true;
+        k = kWin + 1;
+      } else {
+        k = q + 1;
+      }
+    }
+    if (done) break;
+    j -= k;  // first tile not yet published (or the next window)
+    if (k < kWin) {
+      if (++polls > lb.spin_limit) {
         failed = true;
         break;
       }
-      if (spins > 16) __nanosleep(spins > 256 ? 256 : 32);
+      if (polls > 8) __nanosleep(polls > 128 ? 256 : 32);
     }
-    if (failed) break;
-    excl += (uint32_t)w & kCountMask;
-    if (w & kFlagInc) break;
-    --j;
   }
   if (failed) raise_error(ctl, sticky, kErrTimeout);
   st_relaxed_u64(st, tag | kFlagInc | ((excl + agg) & kCountMask));
+  return excl;
+}
+
+// Warp-wide decoupled look-back for one channel: all 32 lanes of a warp call
+// it; lane k reads predecessor (j - k), so each round crosses up to 32 tiles
+// that have published only aggregates. Same publication protocol and bounded
+// waits as lookback_channel. Returns the exclusive prefix in every lane.
+__device__ __forceinline__ uint32_t lookback_warp(const LookbackCfg& lb, uint32_t tile,
+                                                  uint32_t channels, uint32_t c, uint32_t agg,
+                                                  Ctl* ctl, uint32_t* sticky) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint64_t* st = lb.status + (size_t)tile * channels + c;
+  const uint64_t tag = (uint64_t)lb.epoch << 32;
+  if (tile == 0) {
+    if (lane == 0) st_relaxed_u64(st, tag | kFlagInc | agg);
+    return 0;
+  }
+  if (lane == 0) st_relaxed_u64(st, tag | kFlagAgg | agg);
+  uint32_t excl = 0;
+  bool failed = lb.force_timeout != 0;
+  int64_t j = (int64_t)tile - 1;
+  uint32_t polls = 0;
+  while (!failed) {
+    const int64_t idx = j - (int64_t)lane;
+    const uint64_t w = idx >= 0 ? ld_relaxed_u64(lb.status + (size_t)idx * channels + c) : (tag | kFlagInc);
+    const bool ready = (uint32_t)(w >> 32) == lb.epoch && (w & (kFlagAgg | kFlagInc));
+    const uint32_t nr = __ballot_sync(0xffffffffu, !ready);
+    const uint32_t inc = __ballot_sync(0xffffffffu, ready && (w & kFlagInc));
+    const uint32_t stop_nr = nr ? __ffs(nr) - 1 : 32u;
+    const uint32_t stop_inc = inc ? __ffs(inc) - 1 : 32u;
+    const bool found = stop_inc < stop_nr;
+    const uint32_t take = found ? stop_inc + 1 : stop_nr;  // lanes [0, take) are summed
+    uint32_t v = lane < take ? ((uint32_t)w & kCountMask) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    excl += v;
+    if (found) break;
+    j -= take;
+    if (take < 32) {
+      if (++polls > lb.spin_limit) failed = true;
+      else if (polls > 8) __nanosleep(polls > 128 ? 256 : 32);
+    }
+  }
+  if (failed && lane == 0) raise_error(ctl, sticky, kErrTimeout);
+  if (lane == 0) st_relaxed_u64(st, tag | kFlagInc | ((excl + agg) & kCountMask));
   return excl;
 }
 
@@ -374,7 +439,7 @@ const void* reduce_kernel_f32(const ReduceKey& k);
 const void* reduce_kernel_f16(const ReduceKey& k);
 const void* reduce_kernel_bf16(const ReduceKey& k);
 inline size_t reduce_smem_bytes(int kv, int T) {
-  return (size_t)kWarps * kv * 32 * sizeof(float4) + (size_t)(T + 1) * sizeof(uint32_t);
+  return (size_t)kWarps * kv * 32 * sizeof(float4) + 2 * (size_t)(T + 1) * sizeof(uint32_t);
 }
 
 // atomic.cu (the index / offsets check reuses launch_hist with passes = 0)

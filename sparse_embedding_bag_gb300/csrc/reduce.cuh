@@ -71,151 +71,175 @@ struct RowShape {
   int64_t goff;       // column offset of the table in a gradient row
 };
 
+// Lookups gathered per lane group and step, unrolled for memory-level parallelism.
+template <int KV>
+struct Unroll {
+  static constexpr int value = KV >= 8 ? 2 : (KV >= 4 ? 1 : 4 / KV);
+};
+
+// Minimum resident blocks per SM, by vectors per lane (register budget).
+template <int KV>
+struct MinBlocks {
+  static constexpr int value = KV == 1 ? 5 : (KV == 2 ? 4 : (KV == 4 ? 2 : 1));
+};
+
+// Sum over sorted positions [jb, je) of one run into acc by a team of lanes.
+// Within the team, lanes form groups of Lg = 2^rs.lg (one group per lookup,
+// li = lane in group covering vectors li, li+Lg, ...), P groups gather P
+// lookups per step, UNR steps are issued before any result is consumed.
+// `steps` is warp-uniform (teams of one warp may hold runs of different length).
 template <int VK, typename grad_t, int KV>
-__device__ __forceinline__ void gather_one(const ReduceArgs& a, const RowShape& rs,
-                                           typename ValT<VK>::type v, bool ok, uint32_t li,
-                                           float4 (&acc)[KV]) {
+__device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape& rs, uint32_t jb,
+                                            uint32_t je, uint32_t steps, uint32_t P, uint32_t g,
+                                            uint32_t li, float4 (&acc)[KV]) {
+  using V = typename ValT<VK>::type;
+  constexpr int UNR = Unroll<KV>::value;
+  const V* vals = reinterpret_cast<const V*>(a.vals);
   const grad_t* grad = static_cast<const grad_t*>(a.grad);
-  const grad_t* row;
-  float scale = 1.0f;
-  if constexpr (VK == VK_NOBAG) {
-    row = grad + (int64_t)(uint32_t)v * a.grad_stride;
-  } else {
-    const uint32_t bt = (uint32_t)v;
-    const uint32_t b = bt - rs.t * a.B;
-    row = grad + (int64_t)b * a.grad_stride + rs.goff;
-    if constexpr (VK == VK_BAG_SCALED) scale = __uint_as_float((uint32_t)(v >> 32));
-  }
   const uint32_t Lg = 1u << rs.lg;
-  float4 x[KV];
 #pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    const uint32_t u = li + k * Lg;
-    if (ok && u < rs.cvec) x[k] = Vec4<grad_t>::load(row + (int64_t)(rs.cvec_off + u) * 4);
-    else x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t s = 0; s < steps; ++s) {
+    V v[UNR];
+    bool ok[UNR];
 #pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    if constexpr (VK == VK_BAG_SCALED) acc[k] = f4_fma(scale, x[k], acc[k]);
-    else acc[k] = f4_add(x[k], acc[k]);
+    for (int u = 0; u < UNR; ++u) {
+      const uint32_t j = jb + (s * UNR + u) * P + g;
+      ok[u] = j < je;
+      v[u] = ok[u] ? vals[j] : (V)0;
+    }
+    float4 x[UNR][KV];
+    float scale[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const grad_t* row;
+      scale[u] = 1.0f;
+      if constexpr (VK == VK_NOBAG) {
+        row = grad + (int64_t)(uint32_t)v[u] * a.grad_stride;
+      } else {
+        const uint32_t b = (uint32_t)v[u] - rs.t * a.B;
+        row = grad + (int64_t)b * a.grad_stride + rs.goff;
+        if constexpr (VK == VK_BAG_SCALED) scale[u] = __uint_as_float((uint32_t)(v[u] >> 32));
+      }
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const uint32_t q = li + k * Lg;
+        x[u][k] = (ok[u] && q < rs.cvec) ? Vec4<grad_t>::load(row + (int64_t)(rs.cvec_off + q) * 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        if constexpr (VK == VK_BAG_SCALED) acc[k] = f4_fma(scale[u], x[u][k], acc[k]);
+        else acc[k] = f4_add(x[u][k], acc[k]);
+      }
+    }
   }
 }
 
-// Sum over sorted positions [jb, je) of the run into acc (every lane group ends
-// with the same totals). Lookups are taken 32 at a time; 32/Lg are gathered in
-// parallel, two rounds unrolled for memory-level parallelism.
-template <int VK, typename grad_t, int KV>
-__device__ __forceinline__ void warp_gather_sum(const ReduceArgs& a, const RowShape& rs,
-                                                uint32_t jb, uint32_t je, float4 (&acc)[KV]) {
-  using V = typename ValT<VK>::type;
-  const V* vals = reinterpret_cast<const V*>(a.vals);
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t P = 32u >> rs.lg;
-  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
-#pragma unroll
-  for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (uint32_t j0 = jb; j0 < je; j0 += 32) {
-    const uint32_t n = min(32u, je - j0);
-    const V v = lane < n ? vals[j0 + lane] : (V)0;
-    for (uint32_t s = 0; s < n; s += 2 * P) {
-      const uint32_t s0 = s + g, s1 = s + P + g;
-      const V v0 = __shfl_sync(0xffffffffu, v, s0 & 31);
-      const V v1 = __shfl_sync(0xffffffffu, v, s1 & 31);
-      gather_one<VK, grad_t, KV>(a, rs, v0, s0 < n, li, acc);
-      gather_one<VK, grad_t, KV>(a, rs, v1, s1 < n, li, acc);
-    }
-  }
-#pragma unroll
-  for (uint32_t off = 1u << rs.lg; off < 32; off <<= 1) {
+// Adds up the groups of a team (xor over lane offsets Lg .. Lt/2): afterwards
+// every group of the team holds the run's totals. Shuffles are warp-uniform.
+template <int KV>
+__device__ __forceinline__ void team_fold(float4 (&acc)[KV], uint32_t Lg, uint32_t Lt) {
+  for (uint32_t off = 1; off < Lt; off <<= 1) {
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
-      acc[k].x += __shfl_xor_sync(0xffffffffu, acc[k].x, off);
-      acc[k].y += __shfl_xor_sync(0xffffffffu, acc[k].y, off);
-      acc[k].z += __shfl_xor_sync(0xffffffffu, acc[k].z, off);
-      acc[k].w += __shfl_xor_sync(0xffffffffu, acc[k].w, off);
+      float4 y;
+      y.x = __shfl_xor_sync(0xffffffffu, acc[k].x, off);
+      y.y = __shfl_xor_sync(0xffffffffu, acc[k].y, off);
+      y.z = __shfl_xor_sync(0xffffffffu, acc[k].z, off);
+      y.w = __shfl_xor_sync(0xffffffffu, acc[k].w, off);
+      if (off >= Lg) acc[k] = f4_add(y, acc[k]);
     }
   }
 }
 
 template <typename emb_t, int KV>
-__device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs, float4 (&w)[KV]) {
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
-  const emb_t* row = static_cast<const emb_t*>(a.weights) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+__device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs, bool active,
+                                         uint32_t g, uint32_t li, float4 (&w)[KV]) {
+  const emb_t* row = static_cast<const emb_t*>(a.weights) +
+                     (active ? __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D : 0);
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
-    const uint32_t u = li + (k << rs.lg);
-    if (g == 0 && u < rs.cvec) w[k] = Vec4<emb_t>::load_plain(row + (int64_t)(rs.cvec_off + u) * 4);
+    const uint32_t q = li + (k << rs.lg);
+    if (active && g == 0 && q < rs.cvec) w[k] = Vec4<emb_t>::load_plain(row + (int64_t)(rs.cvec_off + q) * 4);
     else w[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
-// Optimizer update of the chunk held by lane group 0 (acc = G, w = old weights).
+// Optimizer update of the chunk held by lane group 0 of a team of Lt lanes
+// (acc = G, w = old weights, tl = lane in team). Warp-uniform shuffles.
 template <typename emb_t, int OPT, int KV>
-__device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& rs,
+__device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& rs, bool active,
+                                           uint32_t g, uint32_t li, uint32_t tl, uint32_t Lt,
                                            const float4 (&acc)[KV], const float4 (&w)[KV],
                                            float m_old) {
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
   float mult = a.lr;
   if constexpr (OPT == 1) {
     float ss = 0.f;
-    if (g == 0) {
+    if (active && g == 0) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
-        const uint32_t u = li + (k << rs.lg);
-        if (u < rs.cvec) ss += acc[k].x * acc[k].x + acc[k].y * acc[k].y + acc[k].z * acc[k].z + acc[k].w * acc[k].w;
+        const uint32_t q = li + (k << rs.lg);
+        if (q < rs.cvec) ss += acc[k].x * acc[k].x + acc[k].y * acc[k].y + acc[k].z * acc[k].z + acc[k].w * acc[k].w;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    for (uint32_t off = 1; off < Lt; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float m_new = m_old + __fdiv_rn(ss, (float)rs.D);
     mult = __fdiv_rn(a.lr, __fsqrt_rn(m_new) + a.eps);
-    if (lane == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
+    if (active && tl == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
   }
+  if (!active || g != 0) return;
   emb_t* row = static_cast<emb_t*>(a.weights) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
-    const uint32_t u = li + (k << rs.lg);
-    if (g == 0 && u < rs.cvec) {
+    const uint32_t q = li + (k << rs.lg);
+    if (q < rs.cvec) {
       const float4 n = make_float4(fmaf(-mult, acc[k].x, w[k].x), fmaf(-mult, acc[k].y, w[k].y),
                                    fmaf(-mult, acc[k].z, w[k].z), fmaf(-mult, acc[k].w, w[k].w));
-      Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + u) * 4, n);
+      Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + q) * 4, n);
     }
   }
 }
 
 template <int KV>
-__device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* s_hsc, uint32_t key,
-                                           uint32_t c, RowShape* rs) {
+__device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* s_hsc,
+                                           const int32_t* s_Do, uint32_t key, uint32_t c,
+                                           RowShape* rs) {
   rs->t = table_of(s_hsc, a.T, key);
   rs->idx = (int64_t)(key - s_hsc[rs->t]);
-  const int32_t d0 = __ldg(&a.D_offsets[rs->t]), d1 = __ldg(&a.D_offsets[rs->t + 1]);
+  const int32_t d0 = s_Do[rs->t], d1 = s_Do[rs->t + 1];
   rs->D = (uint32_t)(d1 - d0);
   rs->goff = d0;
   const uint32_t nvec = rs->D >> 2;
   rs->cvec_off = c * (KV * 32);
-  if (rs->cvec_off >= nvec) return false;
-  rs->cvec = min((uint32_t)(KV * 32), nvec - rs->cvec_off);
+  rs->cvec = rs->cvec_off < nvec ? min((uint32_t)(KV * 32), nvec - rs->cvec_off) : 0u;
   rs->lg = log2_pow2ceil32(rs->cvec);
-  return true;
+  return rs->cvec != 0;
 }
 
 template <typename emb_t, typename grad_t, int OPT, int VK, int KV>
-__global__ void __launch_bounds__(kThreads) k_reduce(ReduceArgs a) {
+__global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(ReduceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float4* s_red = reinterpret_cast<float4*>(smem);                       // [8][KV*32]
+  float4* s_red = reinterpret_cast<float4*>(smem);                          // [8][KV*32]
   uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_red + kWarps * KV * 32);  // [T+1]
+  int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);              // [T+1]
   __shared__ uint32_t s_item, s_last;
+  constexpr int UNR = Unroll<KV>::value;
 
   pdl_wait();
   pdl_trigger();
   if (*(volatile uint32_t*)&a.ctl->err) return;  // a check failed earlier in this call
-  for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) s_hsc[i] = a.hsc[i];
+  for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) {
+    s_hsc[i] = a.hsc[i];
+    s_Do[i] = a.D_offsets[i];
+  }
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t C = a.C;
 
-  // ---- phase 1: block work items of long runs (dynamic).
+  // ---- phase 1: block work items of long runs (dynamic), one warp = one team.
   const uint64_t total_items = (uint64_t)(*(volatile uint32_t*)&a.ctl->num_items) * C;
   for (;;) {
     if (threadIdx.x == 0) s_item = atomicAdd(&a.ctl->item_ctr, 1u);
@@ -231,18 +255,21 @@ __global__ void __launch_bounds__(kThreads) k_reduce(ReduceArgs a) {
     const uint32_t p = w - a.item_base[kl];
     const uint32_t ps = start + p * a.part, pe = min(ps + a.part, end);
     RowShape rs;
-    const bool active = make_shape<KV>(a, s_hsc, a.run_key[r], c, &rs);
+    const bool active = make_shape<KV>(a, s_hsc, s_Do, a.run_key[r], c, &rs);
     if (active) {
       const uint32_t per = (pe - ps + kWarps - 1) / kWarps;
       const uint32_t wb = min(ps + warp * per, pe), we = min(wb + per, pe);
-      float4 acc[KV];
-      warp_gather_sum<VK, grad_t, KV>(a, rs, wb, we, acc);
+      const uint32_t Pg = 32u >> rs.lg;
       const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+      const uint32_t steps = (we - wb + Pg * UNR - 1) / (Pg * UNR);
+      float4 acc[KV];
+      team_gather<VK, grad_t, KV>(a, rs, wb, we, steps, Pg, g, li, acc);
+      team_fold<KV>(acc, 1u << rs.lg, 32);
       if (g == 0) {
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-          const uint32_t u = li + (k << rs.lg);
-          if (u < rs.cvec) s_red[warp * KV * 32 + u] = acc[k];
+          const uint32_t q = li + (k << rs.lg);
+          if (q < rs.cvec) s_red[warp * KV * 32 + q] = acc[k];
         }
       }
     }
@@ -283,39 +310,58 @@ __global__ void __launch_bounds__(kThreads) k_reduce(ReduceArgs a) {
     }
     __syncthreads();
     if (finish && warp == 0) {
-      const uint32_t li = lane & ((1u << rs.lg) - 1);
+      const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
       float4 acc[KV], wv[KV];
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
-        const uint32_t u = li + (k << rs.lg);
-        acc[k] = u < rs.cvec ? s_red[u] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t q = li + (k << rs.lg);
+        acc[k] = q < rs.cvec ? s_red[q] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      load_row<emb_t, KV>(a, rs, wv);
+      load_row<emb_t, KV>(a, rs, true, g, li, wv);
       float m_old = 0.f;
       if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
-      update_row<emb_t, OPT, KV>(a, rs, acc, wv, m_old);
+      update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
     }
     __syncthreads();
   }
 
-  // ---- phase 2: one warp per short run (static stride over runs x chunks).
+  // ---- phase 2: short runs; a warp holds 32/Lt teams of Lt lanes, one run (x chunk) each.
   const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
   const uint64_t tasks = (uint64_t)U * C;
-  const uint64_t W = (uint64_t)gridDim.x * kWarps;
-  for (uint64_t task = (uint64_t)blockIdx.x * kWarps + warp; task < tasks; task += W) {
-    const uint32_t r = C == 1 ? (uint32_t)task : (uint32_t)(task / C);
-    const uint32_t c = (uint32_t)(task - (uint64_t)r * C);
-    const uint32_t start = a.run_start[r], end = a.run_start[r + 1];
-    if (end - start >= a.thr) continue;
-    RowShape rs;
-    if (!make_shape<KV>(a, s_hsc, a.run_key[r], c, &rs)) continue;
+  const uint32_t Lt = 1u << a.team_log2, NT = 32u >> a.team_log2;
+  const uint32_t team = lane >> a.team_log2, tl = lane & (Lt - 1);
+  const uint64_t stride = (uint64_t)gridDim.x * kWarps * NT;
+  for (uint64_t base = ((uint64_t)blockIdx.x * kWarps + warp) * NT; base < tasks; base += stride) {
+    const uint64_t task = base + team;
+    bool active = task < tasks;
+    uint32_t start = 0, end = 0;
+    RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
+    if (active) {
+      const uint32_t r = C == 1 ? (uint32_t)task : (uint32_t)(task / C);
+      const uint32_t c = (uint32_t)(task - (uint64_t)r * C);
+      start = a.run_start[r];
+      end = a.run_start[r + 1];
+      active = end - start < a.thr && make_shape<KV>(a, s_hsc, s_Do, a.run_key[r], c, &rs);
+    }
+    if (!__any_sync(0xffffffffu, active)) continue;
+    if (!active) {
+      rs = RowShape{0u, 0, 4u, 0u, 0u, 0u, 0};
+      start = end = 0;
+    }
+    const uint32_t Pt = Lt >> rs.lg;
+    const uint32_t g = tl >> rs.lg, li = tl & ((1u << rs.lg) - 1);
     float4 wv[KV];
-    load_row<emb_t, KV>(a, rs, wv);
+    load_row<emb_t, KV>(a, rs, active, g, li, wv);
     float m_old = 0.f;
-    if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+    if constexpr (OPT == 1) {
+      if (active) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+    }
+    const uint32_t my_steps = (end - start + Pt * UNR - 1) / (Pt * UNR);
+    const uint32_t steps = __reduce_max_sync(0xffffffffu, my_steps);
     float4 acc[KV];
-    warp_gather_sum<VK, grad_t, KV>(a, rs, start, end, acc);
-    update_row<emb_t, OPT, KV>(a, rs, acc, wv, m_old);
+    team_gather<VK, grad_t, KV>(a, rs, start, end, steps, Pt, g, li, acc);
+    team_fold<KV>(acc, 1u << rs.lg, Lt);
+    update_row<emb_t, OPT, KV>(a, rs, active, g, li, tl, Lt, acc, wv, m_old);
   }
 }
 

@@ -51,7 +51,10 @@ __global__ void __launch_bounds__(kThreads) k_rle(RleArgs a) {
   }
   uint32_t total;
   const uint32_t excl_thread = block_excl_scan(__popc(heads), s_scan, &total);
-  if (threadIdx.x == 0) s_base = lookback_channel(a.lb, tile, 1, 0, total, a.ctl, a.sticky);
+  if (threadIdx.x < 32) {
+    const uint32_t b = lookback_warp(a.lb, tile, 1, 0, total, a.ctl, a.sticky);
+    if (threadIdx.x == 0) s_base = b;
+  }
   __syncthreads();
   const uint32_t base = s_base;
   uint32_t r = base + excl_thread;
@@ -110,9 +113,11 @@ __global__ void __launch_bounds__(kThreads) k_long(LongArgs a) {
     const uint32_t e_long = block_excl_scan(n_long, s_scan, &t_long);
     const uint32_t e_items = block_excl_scan(n_items, s_scan, &t_items);
     const uint32_t e_slots = block_excl_scan(n_slots, s_scan, &t_slots);
-    if (threadIdx.x < 3) {
-      const uint32_t agg = threadIdx.x == 0 ? t_long : (threadIdx.x == 1 ? t_items : t_slots);
-      s_base[threadIdx.x] = lookback_channel(a.lb, tile, 3, threadIdx.x, agg, a.ctl, a.sticky);
+    const uint32_t warp = threadIdx.x >> 5;
+    if (warp < 3) {  // one warp per channel
+      const uint32_t agg = warp == 0 ? t_long : (warp == 1 ? t_items : t_slots);
+      const uint32_t b = lookback_warp(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);
+      if ((threadIdx.x & 31) == 0) s_base[warp] = b;
     }
     __syncthreads();
     uint32_t kl = s_base[0] + e_long, ki = s_base[1] + e_items, ks = s_base[2] + e_slots;

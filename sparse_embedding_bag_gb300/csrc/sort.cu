@@ -23,13 +23,14 @@ template <int ITEMS>
 __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
   constexpr int TILE = kThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem);           // [passes][256]
-  uint32_t* s_bag = s_hist + kMaxPasses * kRadix;                  // [TILE]
+  constexpr int HW = kMaxPasses * kRadix;                          // one warp's histograms
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem);           // [8 warps][passes][256]
+  uint32_t* s_bag = s_hist + kWarps * HW;                          // [TILE]
   uint32_t* s_hsc = s_bag + TILE;                                  // [T+1]
   const DecodeArgs& d = a.d;
   pdl_wait();
   pdl_trigger();
-  for (int i = threadIdx.x; i < kMaxPasses * kRadix; i += kThreads) s_hist[i] = 0;
+  // s_hist first holds the staged bag offsets; it is zeroed after the expansion.
   for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
 
   // CSR validation: non-decreasing offsets from 0 to N.
@@ -43,8 +44,19 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
   const int64_t i0 = (int64_t)blockIdx.x * TILE;
   const int64_t i1 = min(i0 + TILE, d.N);
   __syncthreads();
-  expand_tile_bags(d, i0, i1, s_bag, nullptr);
+  uint32_t bt_lo, bt_hi;
+  expand_tile_bags(d, i0, i1, s_bag, nullptr, reinterpret_cast<int64_t*>(s_hist), kWarps * HW / 2,
+                   &bt_lo, &bt_hi);
+  for (int i = threadIdx.x; i < kWarps * HW; i += kThreads) s_hist[i] = 0;
+  if (threadIdx.x == 0) {  // the first radix pass reuses the tile's bag range
+    a.tile_bags[2 * blockIdx.x] = bt_lo;
+    a.tile_bags[2 * blockIdx.x + 1] = bt_hi;
+  }
+  __syncthreads();
 
+  // Per-warp private histograms in shared memory: plain shared atomics, no
+  // contention between warps; colliding lanes of one warp are serialised.
+  uint32_t* wh = s_hist + (threadIdx.x >> 5) * HW;
   bool any_bad = false;
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
@@ -57,17 +69,15 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
       key = linear_key(d, s_hsc, pos, s_bag[pos - i0], &t, &bad);
       any_bad |= bad;
     }
-    const uint32_t vmask = __ballot_sync(kFull, valid);
-    for (int p = 0; p < a.passes; ++p) {
-      const uint32_t digit = valid ? ((key >> (p * kRadixBits)) & (kRadix - 1)) : 0xffffffffu;
-      const uint32_t peers = __match_any_sync(kFull, digit);
-      if (valid && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
-        atomicAdd(&s_hist[p * kRadix + digit], (uint32_t)__popc(peers & vmask));
+    if (valid) {
+      for (int p = 0; p < a.passes; ++p) atomicAdd(&wh[p * kRadix + ((key >> (p * kRadixBits)) & (kRadix - 1))], 1u);
     }
   }
   if (__syncthreads_or(any_bad) && threadIdx.x == 0) raise_error(a.ctl, a.sticky, kErrIndex);
   for (int i = threadIdx.x; i < a.passes * kRadix; i += kThreads) {
-    const uint32_t c = s_hist[i];
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) c += s_hist[w * HW + i];
     if (c) atomicAdd(&a.ctl->hist[0][0] + i, c);
   }
 }
@@ -94,7 +104,9 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
   pdl_trigger();
 
   if (threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
-  for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
+  if constexpr (FIRST < 0) {  // the first pass stages bag offsets in s_whist first
+    for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
+  }
   if constexpr (FIRST >= 0) {
     for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
   }
@@ -104,7 +116,9 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
   const int64_t i1 = min(i0 + TILE, d.N);
 
   if constexpr (FIRST >= 0)
-    expand_tile_bags(d, i0, i1, s_bag, (FIRST == VK_BAG_SCALED && d.mean) ? s_len : nullptr);
+    expand_bag_range(d, i0, i1, a.tile_bags[2 * tile], a.tile_bags[2 * tile + 1], s_bag,
+                     (FIRST == VK_BAG_SCALED && d.mean) ? s_len : nullptr,
+                     reinterpret_cast<int64_t*>(s_whist), kWarps * kRadix / 2);
 
   uint32_t keys[ITEMS];
   V vals[ITEMS];
@@ -136,7 +150,11 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
       }
     }
   }
-  if constexpr (FIRST >= 0) __syncthreads();  // s_bag / s_len are dead before the exchange buffers are used
+  if constexpr (FIRST >= 0) {  // s_bag / s_len / staged offsets are dead from here on
+    __syncthreads();
+    for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
+    __syncthreads();
+  }
 
   // Warp-level multisplit ranking: stable within the warp's slice of the tile.
   const uint32_t lt = lanemask_lt();
@@ -202,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
 
 template <int ITEMS>
 size_t hist_smem(int T) {
-  return (kMaxPasses * kRadix + kThreads * ITEMS + T + 1) * sizeof(uint32_t);
+  return (kWarps * kMaxPasses * kRadix + kThreads * ITEMS + T + 1) * sizeof(uint32_t);
 }
 
 template <int ITEMS, typename V>
