@@ -142,6 +142,33 @@ emb_status emb_nobag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indic
                              const void* grad_output, float lr, emb_nobag_path path,
                              void* stream);
 
+/* Allocation-free unpooled atomic SGD (the same update as emb_nobag_bwd_sgd with
+ * EMB_NOBAG_ATOMIC), for callers that cannot allocate device memory when they run
+ * it: inside a CUDA graph capture, under a runtime that owns all device memory,
+ * or where the library must not call the device allocator. The pages have no
+ * counterpart of this entry point; it exists for those callers.
+ *   No plan is used and nothing is allocated (no cudaMalloc, cudaFree or
+ *   allocating library call). Scratch is one fixed static device array in the
+ *   library image, about 53 KB, present on every GPU that loads the library
+ *   until the process exits. Limits: N <= 4194304 lookups, T <= 4096 tables,
+ *   B*T < 2^31, D a multiple of 4 and <= 4096; beyond them EMB_ERR_INVALID_ARG.
+ *   hash_size_cumsum (int64[T+1]) and weights_offsets (int64[T]) are caller-owned
+ *   DEVICE arrays here; weights are fp32; grad_output is [N, D] of grad_dtype.
+ *   device_status (device uint32, may be NULL) receives this call's device error
+ *   bits: 1 = an index outside its table, 2 = malformed offsets or
+ *   hash_size_cumsum; 0 = none. Nothing is updated when a bit is set.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the scratch array: calls that overlap on the GPU race, so
+ *   order them (one stream, or events). Asynchronous on `stream`. */
+emb_status emb_nobag_bwd_sgd_atomic_noalloc(int device, int32_t T,
+                                            const int64_t* hash_size_cumsum,
+                                            const int64_t* weights_offsets, int32_t D,
+                                            float* weights, const int64_t* indices,
+                                            const int64_t* offsets, int64_t N, int32_t B,
+                                            const void* grad_output, emb_dtype grad_dtype,
+                                            float lr, uint32_t* device_status, void* stream);
+
 /* Waits for the plan's last call, then returns and clears the latched device
  * error (EMB_OK if none). */
 emb_status emb_plan_status(emb_plan* plan);

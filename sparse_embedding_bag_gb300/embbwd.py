@@ -27,7 +27,7 @@ EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 # Every symbol include/embbwd.h declares (checked by the tests against the header).
 EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_rowwise_adagrad",
            "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
-           "emb_plan_stage_ms", "emb_status_string")
+           "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,8 @@ def load(path: str = LIB_PATH):
             "emb_plan_set_profiling": [vp, c_int],
             "emb_plan_stage_ms": [vp, vp, i32],
             "emb_status_string": [c_int],
+            "emb_nobag_bwd_sgd_atomic_noalloc": [c_int, i32, vp, vp, i32, vp, vp, vp, i64, i32, vp,
+                                                 c_int, f32, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -182,3 +184,15 @@ def emb_plan_stage_ms(plan, n=5):
     out = np.zeros(n, np.float32)
     _check(load().emb_plan_stage_ms(plan, out.ctypes.data, n), "emb_plan_stage_ms")
     return out
+
+
+def emb_nobag_bwd_sgd_atomic_noalloc(device, T, hash_size_cumsum, weights_offsets, D, weights,
+                                     indices, offsets, N, B, grad_output, grad_dtype, lr,
+                                     device_status=None, stream=None):
+    """Allocation-free unpooled atomic SGD; table arrays are device tensors (int64)."""
+    st = load().emb_nobag_bwd_sgd_atomic_noalloc(int(device), int(T), _ptr(hash_size_cumsum),
+                                                 _ptr(weights_offsets), int(D), _ptr(weights),
+                                                 _ptr(indices), _ptr(offsets), int(N), int(B),
+                                                 _ptr(grad_output), int(grad_dtype), float(lr),
+                                                 _ptr(device_status), _stream(stream))
+    return _check(st, "emb_nobag_bwd_sgd_atomic_noalloc")

@@ -1,0 +1,98 @@
+"""The allocation-free entry point, emb_nobag_bwd_sgd_atomic_noalloc.
+
+It serves callers that cannot allocate device memory when they run the update
+(inside a CUDA graph capture, under a runtime that owns all device memory, or
+where the library must not call the device allocator): no plan, scratch in a
+fixed static device array. This file is collected last so that a run stopping
+at its first failure has already run every other test.
+
+Checked through the C ABI against the existing entry point (a plan plus
+emb_nobag_bwd_sgd with the atomic path), within the parity tolerance, on two
+calls in a row each, so that the shared scratch being left over from the
+previous call is exercised.
+"""
+import numpy as np
+import pytest
+
+from sparse_embedding_bag_gb300 import device as dev
+from sparse_embedding_bag_gb300 import embbwd as E
+from sparse_embedding_bag_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 1e-4, 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from sparse_embedding_bag_gb300 import build
+    build.build()
+    E.load()
+
+
+def _workload(seed, grad_dtype=synth.F32):
+    rng = np.random.default_rng(seed)
+    rows, D, B = [700, 3000, 45], 64, 16
+    return synth.make_bag_workload(
+        "noalloc", seed, rows, [D] * 3, B, rng.integers(0, 60, (3, B)),
+        lambda r, t, n: synth.sample_zipf(r, rows[t], 1.1, n), nobag=True, grad_dtype=grad_dtype)
+
+
+@pytest.mark.parametrize("grad_dtype", [synth.F32, synth.BF16])
+def test_noalloc_matches_planned_atomic_path_twice(grad_dtype):
+    import torch
+    w = _workload(11, grad_dtype)
+    ref = dev.to_device(w)
+    new = dev.to_device(w)
+    hsc = torch.from_numpy(w.hash_size_cumsum).cuda()
+    wo = torch.from_numpy(w.weights_offsets).cuda()
+    status = torch.full((1,), 0xFFFF, dtype=torch.int32, device="cuda")
+    plan = dev.make_plan(w)
+    try:
+        for _ in range(2):
+            E.emb_nobag_bwd_sgd(plan, ref.weights, ref.indices, ref.offsets, w.N, w.B,
+                                ref.grad_output, w.lr, E.EMB_NOBAG_ATOMIC)
+            E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, int(w.dims[0]), new.weights,
+                                               new.indices, new.offsets, w.N, w.B,
+                                               new.grad_output, w.grad_dtype, w.lr, status)
+            torch.cuda.synchronize()
+            assert E.emb_plan_status(plan) == E.EMB_OK
+            assert int(status.item()) == 0
+            np.testing.assert_allclose(new.weights.cpu().numpy(), ref.weights.cpu().numpy(),
+                                       rtol=RTOL, atol=ATOL)
+    finally:
+        E.emb_plan_destroy(plan)
+    assert not np.array_equal(new.weights.cpu().numpy(), w.weights)  # it did update
+
+
+def test_noalloc_reports_errors_and_limits():
+    import torch
+    w = _workload(12)
+    d = dev.to_device(w)
+    hsc = torch.from_numpy(w.hash_size_cumsum).cuda()
+    wo = torch.from_numpy(w.weights_offsets).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    D = int(w.dims[0])
+    # beyond the stated maximum number of lookups: rejected on the host
+    with pytest.raises(E.EmbError) as e:
+        E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, D, d.weights, d.indices, d.offsets,
+                                           (1 << 22) + 1, w.B, d.grad_output, w.grad_dtype, w.lr,
+                                           status)
+    assert e.value.status == E.EMB_ERR_INVALID_ARG
+    # an index outside its table: reported in device_status, nothing updated
+    bad = d.indices.clone()
+    bad[w.N // 2] = 10**9
+    before = d.weights.clone()
+    E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, D, d.weights, bad, d.offsets, w.N, w.B,
+                                       d.grad_output, w.grad_dtype, w.lr, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+    assert torch.equal(d.weights, before)
+    # the next valid call starts clean
+    E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, D, d.weights, d.indices, d.offsets, w.N,
+                                       w.B, d.grad_output, w.grad_dtype, w.lr, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert not torch.equal(d.weights, before)
