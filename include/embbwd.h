@@ -149,7 +149,7 @@ emb_status emb_nobag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indic
  * counterpart of this entry point; it exists for those callers.
  *   No plan is used and nothing is allocated (no cudaMalloc, cudaFree or
  *   allocating library call). Scratch is one fixed static device array in the
- *   library image, about 53 KB, present on every GPU that loads the library
+ * library image, about 21 KB, present on every GPU that loads the library
  *   until the process exits. Limits: N <= 4194304 lookups, T <= 4096 tables,
  *   B*T < 2^31, D a multiple of 4 and <= 4096; beyond them EMB_ERR_INVALID_ARG.
  *   hash_size_cumsum (int64[T+1]) and weights_offsets (int64[T]) are caller-owned

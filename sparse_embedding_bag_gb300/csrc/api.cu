@@ -73,13 +73,10 @@ struct emb_plan {
   uint32_t* keys[2] = {nullptr, nullptr};
   void* vals[2] = {nullptr, nullptr};
   uint64_t* status = nullptr;
-  uint32_t* tile_bags = nullptr;
   uint32_t* run_key = nullptr;
   uint32_t* run_start = nullptr;
   uint32_t* long_ids = nullptr;
-  uint32_t* item_base = nullptr;
-  uint32_t* slot_base = nullptr;
-  uint32_t* item_long = nullptr;
+  Item* items = nullptr;
   float4* partials = nullptr;
   uint32_t* done = nullptr;
   uint32_t cap_long = 0, cap_items = 0, cap_slots = 0;
@@ -186,17 +183,17 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
 
   EMB_TRY(record(p, 0, s));
   EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
-  HistArgs ha{d, p->ctl, p->sticky, passes, tile, p->tile_bags};
-  EMB_CUDA(launch_hist(ha, p->T, s, pdl));
+  // the linearised pairs go to buffer 1, which the first pass reads
+  HistArgs ha{d, p->ctl, p->sticky, passes, tile, p->keys[1], p->vals[1]};
+  EMB_CUDA(launch_hist(ha, vk, p->T, s, pdl));
   EMB_TRY(record(p, 1, s));
   for (int pass = 0; pass < passes; ++pass) {
     PassArgs pa;
-    pa.d = d;
+    pa.N = N;
     pa.ctl = p->ctl;
     pa.sticky = p->sticky;
     pa.lb = lb0;
     pa.lb.epoch = epoch + (uint32_t)pass;
-    pa.tile_bags = p->tile_bags;
     const int in = (pass + 1) & 1, out = pass & 1;
     pa.keys_in = p->keys[in];
     pa.vals_in = p->vals[in];
@@ -204,32 +201,28 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_out = p->vals[out];
     pa.pass = pass;
     pa.shift = pass * kRadixBits;
-    EMB_CUDA(launch_sort_pass(pa, pass == 0 ? vk : -1, wide, tile, p->T, s, pdl));
+    EMB_CUDA(launch_sort_pass(pa, wide, tile, s, pdl));
   }
   const int fin = (passes - 1) & 1;
   EMB_TRY(record(p, 2, s));
-  RleArgs ra{p->keys[fin], N, p->ctl, p->sticky, lb0, p->run_key, p->run_start};
+  RunsArgs ra;
+  ra.keys = p->keys[fin];
+  ra.N = N;
+  ra.ctl = p->ctl;
+  ra.sticky = p->sticky;
+  ra.lb = lb0;
   ra.lb.epoch = epoch + 5;
-  EMB_CUDA(launch_rle(ra, s, pdl));
-  EMB_TRY(record(p, 3, s));
-  LongArgs la;
-  la.ctl = p->ctl;
-  la.sticky = p->sticky;
-  la.lb = lb0;
-  la.lb.epoch = epoch + 6;
-  la.run_start = p->run_start;
-  la.thr = p->thr;
-  la.part = part_for(p, N);
-  la.long_ids = p->long_ids;
-  la.item_base = p->item_base;
-  la.slot_base = p->slot_base;
-  la.item_long = p->item_long;
-  la.cap_long = p->cap_long;
-  la.cap_items = p->cap_items;
-  la.cap_slots = p->cap_slots;
-  const int64_t long_tiles = (N + kLongTile - 1) / kLongTile;
-  const int long_grid = (int)std::min<int64_t>(long_tiles, 2 * (int64_t)p->props.sms);
-  EMB_CUDA(launch_long(la, long_grid, s, pdl));
+  ra.run_key = p->run_key;
+  ra.run_start = p->run_start;
+  ra.thr = p->thr;
+  ra.part = part_for(p, N);
+  ra.long_ids = p->long_ids;
+  ra.items = p->items;
+  ra.cap_long = p->cap_long;
+  ra.cap_items = p->cap_items;
+  ra.cap_slots = p->cap_slots;
+  EMB_CUDA(launch_runs(ra, s, pdl));
+  EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel
   EMB_TRY(record(p, 4, s));
 
   ReduceArgs r;
@@ -237,10 +230,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.vals = static_cast<const uint32_t*>(p->vals[fin]);
   r.run_key = p->run_key;
   r.run_start = p->run_start;
-  r.long_ids = p->long_ids;
-  r.item_base = p->item_base;
-  r.slot_base = p->slot_base;
-  r.item_long = p->item_long;
+  r.items = p->items;
   r.partials = p->partials;
   r.done = p->done;
   r.grad = grad;
@@ -256,7 +246,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.lr = lr;
   r.eps = eps;
   r.thr = p->thr;
-  r.part = la.part;
+  r.part = ra.part;
   r.C = p->C;
   r.team_log2 = p->team_log2;
   const void* fn = reduce_fn(p, opt, vk);
@@ -361,8 +351,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   // ---- scratch sizes
   const uint64_t N = (uint64_t)std::max<int64_t>(max_N, 1);
   const uint64_t sort_tiles = std::max<uint64_t>((N + 1023) / 1024, 1);  // smallest tile is 1024
-  const uint64_t status_words = std::max<uint64_t>(
-      sort_tiles * kRadix, std::max<uint64_t>((N + kRleTile - 1) / kRleTile, (N + kLongTile - 1) / kLongTile * 3));
+  const uint64_t status_words = std::max<uint64_t>(sort_tiles * kRadix, (N + kRleTile - 1) / kRleTile * 4);
   // part_for(N) >= N / (2 * sms * 32) and >= base_part, so no call has more than
   // max(N / kMaxPart, 2 * sms * 32) long-run parts beyond one per long run.
   const uint64_t parts_bound = std::max<uint64_t>(N / kMaxPart + 1, 2ull * p->props.sms * 32 + 1);
@@ -388,13 +377,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {&p->vals[0], N * sizeof(uint64_t)},
       {&p->vals[1], N * sizeof(uint64_t)},
       {reinterpret_cast<void**>(&p->status), status_words * sizeof(uint64_t)},
-      {reinterpret_cast<void**>(&p->tile_bags), 2 * sort_tiles * sizeof(uint32_t)},
+
       {reinterpret_cast<void**>(&p->run_key), N * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
-      {reinterpret_cast<void**>(&p->item_base), p->cap_long * sizeof(uint32_t)},
-      {reinterpret_cast<void**>(&p->slot_base), p->cap_long * sizeof(uint32_t)},
-      {reinterpret_cast<void**>(&p->item_long), p->cap_items * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->items), p->cap_items * sizeof(Item)},
       {reinterpret_cast<void**>(&p->partials), (size_t)p->cap_slots * p->C * part_row},
       {reinterpret_cast<void**>(&p->done), (size_t)p->cap_slots * p->C * sizeof(uint32_t)},
   };
@@ -514,8 +501,8 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
     const DecodeArgs d = decode_args(p, indices, offsets, nullptr, N, B, 0);
     EMB_TRY(record(p, 0, s));
     EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
-    HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N), p->tile_bags};
-    EMB_CUDA(launch_hist(ha, p->T, s, pdl));
+    HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N), nullptr, nullptr};
+    EMB_CUDA(launch_hist(ha, -1, p->T, s, pdl));
     for (int i = 1; i <= 4; ++i) EMB_TRY(record(p, i, s));
     AtomicArgs aa{d, p->ctl, p->sticky, grad_output, static_cast<float*>(weights), p->d_wo,
                   (uint32_t)p->max_D, lr};

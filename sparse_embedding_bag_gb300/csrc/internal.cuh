@@ -1,17 +1,17 @@
 // Internal declarations shared by the CUDA translation units of libembbwd.
 //
 // Pipeline of one sorted call (all stream-ordered, no host synchronisation):
-//   memset(ctl) -> k_hist -> k_sort_pass x passes -> k_rle -> k_long -> k_reduce
+//   memset(ctl) -> k_hist -> k_sort_pass x passes -> k_runs -> k_reduce
 //   k_hist      linearises every lookup (hash_size_cumsum[t] + idx), checks it
 //               against its table, validates the CSR offsets and builds the digit
 //               histograms of all radix passes in one read of the indices.
 //   k_sort_pass one LSD radix pass (8-bit digits) with decoupled look-back; the
 //               first pass recomputes the keys from the indices instead of
 //               reading a materialised key array.
-//   k_rle       run-length encode of the sorted keys (unique keys, run starts,
-//               number of runs), one pass with decoupled look-back.
-//   k_long      ordered compaction of runs with >= max_segment_length_per_warp
-//               lookups into block work items (hot rows split into parts).
+//   k_runs      run-length encode of the sorted keys (unique keys, run starts,
+//               number of runs) fused with the ordered compaction of runs with
+//               >= max_segment_length_per_warp lookups into block work items
+//               (hot rows split into parts); one pass, decoupled look-back.
 //   k_reduce    persistent: block-level work items for long runs (multi-block
 //               parts combined in a fixed order), then one warp per short run;
 //               fp32 accumulation of the scaled gradient rows and the optimizer
@@ -22,6 +22,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace embbwd {
 
@@ -43,7 +45,7 @@ constexpr uint32_t kErrTimeout = 4u;
 constexpr uint32_t kErrCapacity = 8u;
 
 // Dynamic tile counters, one per kernel of a call.
-enum TileCounter { TC_PASS0 = 0, TC_RLE = kMaxPasses, TC_LONG = kMaxPasses + 1, TC_COUNT = 8 };
+enum TileCounter { TC_PASS0 = 0, TC_RLE = kMaxPasses, TC_COUNT = 8 };
 
 // Per-call control block, zeroed by one memset at the start of every call.
 struct Ctl {
@@ -95,15 +97,15 @@ struct HistArgs {
   uint32_t* sticky;
   int passes;
   int tile;              // lookups per block
-  uint32_t* tile_bags;   // out: [2 * tiles] first and last bag overlapping each tile
+  uint32_t* keys_out;    // linear keys in lookup order (not written when only checking)
+  void* vals_out;        // payloads in lookup order
 };
 
 struct PassArgs {
-  DecodeArgs d;
+  int64_t N;
   Ctl* ctl;
   uint32_t* sticky;
   LookbackCfg lb;
-  const uint32_t* tile_bags;  // from k_hist (same tile size), used by the first pass
   const uint32_t* keys_in;
   const void* vals_in;
   uint32_t* keys_out;
@@ -112,27 +114,24 @@ struct PassArgs {
   int shift;
 };
 
-struct RleArgs {
+// One block work item of a long run: lookups [ps, pe) of the run with linear
+// index `key`; part q of P. Runs with P > 1 own partial-sum slots slot0 .. slot0+P-1.
+struct __align__(16) Item {
+  uint32_t ps, pe, key, slot0, q, P, pad0, pad1;
+};
+
+struct RunsArgs {
   const uint32_t* keys;  // sorted
   int64_t N;
   Ctl* ctl;
   uint32_t* sticky;
   LookbackCfg lb;
   uint32_t* run_key;
-  uint32_t* run_start;  // [U+1]
-};
-
-struct LongArgs {
-  Ctl* ctl;
-  uint32_t* sticky;
-  LookbackCfg lb;
-  const uint32_t* run_start;
+  uint32_t* run_start;   // [U+1]
   uint32_t thr;
-  uint32_t part;  // lookups per block work item
+  uint32_t part;         // lookups per block work item
   uint32_t* long_ids;
-  uint32_t* item_base;
-  uint32_t* slot_base;
-  uint32_t* item_long;
+  Item* items;
   uint32_t cap_long, cap_items, cap_slots;
 };
 
@@ -141,10 +140,7 @@ struct ReduceArgs {
   const uint32_t* vals;     // sorted values (uint32 or uint64, per value kind)
   const uint32_t* run_key;
   const uint32_t* run_start;
-  const uint32_t* long_ids;
-  const uint32_t* item_base;
-  const uint32_t* slot_base;
-  const uint32_t* item_long;
+  const Item* items;
   float4* partials;         // [slots * C][KV*32]
   uint32_t* done;           // [slots * C]
   const void* grad;
@@ -417,15 +413,13 @@ inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, size_t s
 
 // sort.cu
 size_t sort_tile_for(int64_t N);  // lookups per block for hist and the passes
-cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s, bool pdl);
-cudaError_t launch_sort_pass(const PassArgs& a, int first_kind /* -1: from buffers */,
-                             bool wide_vals, int tile, int T, cudaStream_t s, bool pdl);
+// first_kind: the ValueKind of the pairs to write, or -1 to only check indices and offsets.
+cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s, bool pdl);
+cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl);
 cudaError_t sort_configure(const DevProps& p);
-size_t sort_smem_bytes(int tile, bool wide_vals, bool first, int T);
 
 // runs.cu
-cudaError_t launch_rle(const RleArgs& a, cudaStream_t s, bool pdl);
-cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl);
 
 // reduce_*.cu: one entry per weight type.
 struct ReduceKey {

@@ -6,8 +6,8 @@
 // their own pools, or embedders that forbid the library from touching the
 // device allocator. Every other entry point needs a plan, and creating a plan
 // calls cudaMalloc for its scratch. This one needs no plan: its scratch (the
-// per-call control block, the error word, the 32-bit table offsets and the
-// per-tile bag ranges) is the file-scope array below, which is part of the
+// per-call control block, the error word and the 32-bit table offsets, about
+// 21 KB) is the file-scope array below, which is part of the
 // library's device image: it exists on every GPU that loads the library and
 // stays there until the process exits. Its size bounds the problem:
 // at most kNoAllocMaxN lookups and kMaxT tables per call.
@@ -28,14 +28,12 @@ namespace {
 
 constexpr int64_t kNoAllocMaxN = (int64_t)1 << 22;  // lookups per call
 constexpr int kNoAllocMaxDevices = 64;
-constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxN / 1024 + 1;  // the check kernel's tiles are >= 1024 lookups
 
 struct NoAllocScratch {
   Ctl ctl;              // zeroed each call
   uint32_t status;      // zeroed each call; error bits of this call
   uint32_t pad[63];
   uint32_t hsc[kMaxT + 1];
-  uint32_t tile_bags[2 * kNoAllocMaxTiles];
 };
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
@@ -120,8 +118,8 @@ extern "C" emb_status emb_nobag_bwd_sgd_atomic_noalloc(
     d.mean = 0;
     // index range and CSR checks (no radix histogram), then the atomic scatter,
     // which does nothing if a check failed
-    HistArgs ha{d, &sc->ctl, &sc->status, 0, (int)sort_tile_for(N), sc->tile_bags};
-    if (e == cudaSuccess) e = launch_hist(ha, T, s, false);
+    HistArgs ha{d, &sc->ctl, &sc->status, 0, (int)sort_tile_for(N), nullptr, nullptr};
+    if (e == cudaSuccess) e = launch_hist(ha, -1, T, s, false);
     AtomicArgs aa{d, &sc->ctl, &sc->status, grad_output, weights, weights_offsets, (uint32_t)D, lr};
     if (e == cudaSuccess) e = launch_nobag_atomic(aa, (int)grad_dtype, T, s, false);
   }

@@ -248,14 +248,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
     if (w_all >= total_items) break;
     const uint32_t w = C == 1 ? w_all : w_all / C;
     const uint32_t c = w_all - w * C;
-    const uint32_t kl = a.item_long[w];
-    const uint32_t r = a.long_ids[kl];
-    const uint32_t start = a.run_start[r], end = a.run_start[r + 1];
-    const uint32_t P = (end - start + a.part - 1) / a.part;
-    const uint32_t p = w - a.item_base[kl];
-    const uint32_t ps = start + p * a.part, pe = min(ps + a.part, end);
+    const Item it = a.items[w];
+    const uint32_t P = it.P, p = it.q, ps = it.ps, pe = it.pe;
     RowShape rs;
-    const bool active = make_shape<KV>(a, s_hsc, s_Do, a.run_key[r], c, &rs);
+    const bool active = make_shape<KV>(a, s_hsc, s_Do, it.key, c, &rs);
     if (active) {
       const uint32_t per = (pe - ps + kWarps - 1) / kWarps;
       const uint32_t wb = min(ps + warp * per, pe), we = min(wb + per, pe);
@@ -285,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
       if (P == 1) {
         if (u < rs.cvec) s_red[u] = G;
       } else {
-        const uint32_t slot0 = a.slot_base[kl];
+        const uint32_t slot0 = it.slot0;
         float4* part = a.partials + ((size_t)(slot0 + p) * C + c) * (KV * 32);
         if (u < rs.cvec) part[u] = G;
         __threadfence();

@@ -1,167 +1,195 @@
-// Run-length encoding of the sorted linear indices and the long-run partition.
+// Run-length encoding of the sorted linear indices fused with the long-run
+// partition, in one pass over the sorted keys.
 //
-// k_rle: the unique sorted linear indices, the start of every run (the
-//   exclusive scan of the run lengths) and the number of runs -- the outputs
-//   "fbgemm_gpu/codegen/embedding_backward_split_template.cu" takes from its
-//   transpose step (sorted_linear_indices_run, ..._cumulative_run_lengths,
-//   ..._num_runs). One pass: each block flags run heads in its tile, counts them
-//   and gets the count of all earlier tiles by decoupled look-back.
-// k_long: the set of runs with at least max_segment_length_per_warp lookups
-//   (that page's *_find_long_segments), produced as an ordered compaction
-//   instead of an atomic append, together with the block work items for them:
-//   a run is cut into parts of `part` lookups, and runs with more than one part
-//   get a slot per part for fp32 partial sums that the last part to finish
-//   combines in part order.
+// Outputs, as in "fbgemm_gpu/codegen/embedding_backward_split_template.cu":
+//   * the unique sorted linear indices, the start of every run (the exclusive
+//     scan of the run lengths, last entry N) and the number of runs (that
+//     page's sorted_linear_indices_run / _cumulative_run_lengths / _num_runs);
+//   * the runs with at least max_segment_length_per_warp lookups (that page's
+//     *_find_long_segments), as an ordered compaction instead of an atomic
+//     append, together with their block work items: a long run is cut into
+//     parts of `part` lookups; runs with more than one part get one fp32
+//     partial-sum slot per part, combined later in part order.
+//
+// Each block owns a tile of kRleTile sorted keys and the runs whose first
+// lookup lies in it. A run that continues past the tile end has its end found
+// by a 32-lane parallel upper-bound search (a few rounds of one load per lane),
+// so every run's length is known inside the block that owns it. The four counts
+// (runs, long runs, work items, partial slots) of earlier tiles come from one
+// decoupled look-back per count, each walked 32 tiles at a time by a warp.
 #include "internal.cuh"
 
 namespace embbwd {
 
 namespace {
 
-__global__ void __launch_bounds__(kThreads) k_rle(RleArgs a) {
+// First position >= b whose key differs from k (or N), given that position b-1
+// holds k. Called by all lanes of one warp; every lane gets the answer.
+__device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ keys, uint32_t N,
+                                                   uint32_t b, uint32_t k) {
+  const uint32_t lane = threadIdx.x & 31;
+  if (b >= N) return N;
+  // exponential probe: lane l tests b - 1 + 2^l
+  const uint64_t q = (uint64_t)b - 1 + ((uint64_t)1 << lane);
+  const bool in = lane < 31 && q < N && keys[q] == k;
+  const uint32_t m = __popc(__ballot_sync(0xffffffffu, in));  // lanes 0..m-1 are inside the run
+  if (m == 0) return b;
+  uint64_t lo = (uint64_t)b + ((uint64_t)1 << (m - 1));               // b-1+2^(m-1) is inside
+  const uint64_t cap = (uint64_t)b - 1 + ((uint64_t)1 << m);
+  uint64_t hi = cap < (uint64_t)N ? cap : (uint64_t)N;  // outside, or N
+  while (hi > lo) {  // invariant: positions < lo are inside, position hi is outside (or N)
+    const uint64_t step = (hi - lo + 31) / 32;
+    const uint64_t p = lo + lane * step;
+    const bool inside = p < hi && keys[p] == k;
+    const uint32_t c = __popc(__ballot_sync(0xffffffffu, inside));
+    if (c == 0) break;  // position lo itself is outside
+    const uint64_t nlo = lo + (uint64_t)(c - 1) * step + 1;
+    const uint64_t nhi = lo + (uint64_t)c * step;
+    hi = nhi < hi ? nhi : hi;
+    lo = nlo;
+  }
+  return (uint32_t)lo;
+}
+
+__global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   __shared__ uint32_t s_tile;
   __shared__ uint32_t s_scan[kWarps];
-  __shared__ uint32_t s_base;
+  __shared__ uint32_t s_base[4];
+  __shared__ uint32_t s_last_key;
+  __shared__ uint32_t s_head_pos[kRleTile + 1];
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
   __syncthreads();
   const uint32_t tile = s_tile;
-  const int64_t i0 = (int64_t)tile * kRleTile;
-  const int64_t p0 = i0 + (int64_t)threadIdx.x * kRleItems;
+  const uint32_t N = (uint32_t)a.N;
+  const uint32_t i0 = tile * kRleTile;
+  const uint32_t p0 = i0 + threadIdx.x * kRleItems;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint32_t key[kRleItems];
-  if (p0 + kRleItems <= a.N) {
+  if (p0 + kRleItems <= N) {
     const uint4 u0 = *reinterpret_cast<const uint4*>(a.keys + p0);
     const uint4 u1 = *reinterpret_cast<const uint4*>(a.keys + p0 + 4);
     key[0] = u0.x; key[1] = u0.y; key[2] = u0.z; key[3] = u0.w;
     key[4] = u1.x; key[5] = u1.y; key[6] = u1.z; key[7] = u1.w;
   } else {
 #pragma unroll
-    for (int k = 0; k < kRleItems; ++k) key[k] = p0 + k < a.N ? a.keys[p0 + k] : 0u;
+    for (int k = 0; k < kRleItems; ++k) key[k] = p0 + k < N ? a.keys[p0 + k] : 0u;
   }
-  uint32_t prev = 0;
-  if (p0 > 0 && p0 <= a.N) prev = a.keys[p0 - 1];
+  const uint32_t prev = (p0 > 0 && p0 <= N) ? a.keys[p0 - 1] : 0u;
   uint32_t heads = 0;  // bit k: position p0+k starts a run
 #pragma unroll
   for (int k = 0; k < kRleItems; ++k) {
-    const int64_t p = p0 + k;
     const uint32_t before = k == 0 ? prev : key[k - 1];
-    if (p < a.N && (p == 0 || key[k] != before)) heads |= 1u << k;
+    if (p0 + k < N && (p0 + k == 0 || key[k] != before)) heads |= 1u << k;
   }
-  uint32_t total;
-  const uint32_t excl_thread = block_excl_scan(__popc(heads), s_scan, &total);
-  if (threadIdx.x < 32) {
-    const uint32_t b = lookback_warp(a.lb, tile, 1, 0, total, a.ctl, a.sticky);
-    if (threadIdx.x == 0) s_base = b;
+  uint32_t n_heads;
+  const uint32_t h0 = block_excl_scan(__popc(heads), s_scan, &n_heads);
+  {
+    uint32_t h = h0;
+#pragma unroll
+    for (int k = 0; k < kRleItems; ++k) {
+      if (heads & (1u << k)) {
+        s_head_pos[h] = p0 + k;
+        if (h == n_heads - 1) s_last_key = key[k];
+        ++h;
+      }
+    }
   }
   __syncthreads();
-  const uint32_t base = s_base;
-  uint32_t r = base + excl_thread;
+  // end of the tile's last run (it may continue into later tiles)
+  if (warp == 0 && n_heads > 0) {
+    const uint32_t tile_end = min(i0 + (uint32_t)kRleTile, N);
+    const uint32_t e = run_end_search(a.keys, N, tile_end, s_last_key);
+    if (lane == 0) s_head_pos[n_heads] = e;
+  }
+  __syncthreads();
+
+  // lengths, long runs, parts and partial slots of this thread's runs
+  uint32_t n_long = 0, n_items = 0, n_slots = 0;
+  {
+    uint32_t h = h0;
+#pragma unroll
+    for (int k = 0; k < kRleItems; ++k) {
+      if (heads & (1u << k)) {
+        const uint32_t SL = s_head_pos[h + 1] - s_head_pos[h];
+        if (SL >= a.thr) {
+          const uint32_t P = (SL + a.part - 1) / a.part;
+          n_long += 1;
+          n_items += P;
+          if (P > 1) n_slots += P;
+        }
+        ++h;
+      }
+    }
+  }
+  uint32_t t_long, t_items, t_slots;
+  const uint32_t e_long = block_excl_scan(n_long, s_scan, &t_long);
+  const uint32_t e_items = block_excl_scan(n_items, s_scan, &t_items);
+  const uint32_t e_slots = block_excl_scan(n_slots, s_scan, &t_slots);
+  if (warp < 4) {  // one warp per count
+    const uint32_t agg = warp == 0 ? n_heads : warp == 1 ? t_long : warp == 2 ? t_items : t_slots;
+    const uint32_t b = lookback_warp(a.lb, tile, 4, warp, agg, a.ctl, a.sticky);
+    if (lane == 0) s_base[warp] = b;
+  }
+  __syncthreads();
+
+  uint32_t r = s_base[0] + h0;
+  uint32_t kl = s_base[1] + e_long, ki = s_base[2] + e_items, ks = s_base[3] + e_slots;
+  bool overflow = false;
+  uint32_t h = h0;
 #pragma unroll
   for (int k = 0; k < kRleItems; ++k) {
     if (heads & (1u << k)) {
-      if (r < (uint64_t)a.N) {
+      const uint32_t start = s_head_pos[h], end = s_head_pos[h + 1];
+      if (r < N) {
         a.run_key[r] = key[k];
-        a.run_start[r] = (uint32_t)(p0 + k);
+        a.run_start[r] = start;
+      } else {
+        overflow = true;
       }
-      ++r;
-    }
-  }
-  if (i0 + kRleTile >= a.N && threadIdx.x == 0) {
-    const uint32_t U = base + total;
-    if (U <= (uint64_t)a.N) {
-      a.ctl->num_runs = U;
-      a.run_start[U] = (uint32_t)a.N;
-    } else {
-      raise_error(a.ctl, a.sticky, kErrCapacity);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kThreads) k_long(LongArgs a) {
-  __shared__ uint32_t s_tile;
-  __shared__ uint32_t s_scan[kWarps];
-  __shared__ uint32_t s_base[3];
-  pdl_wait();
-  pdl_trigger();
-  const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
-  for (;;) {
-    if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_LONG], 1u);
-    __syncthreads();
-    const uint32_t tile = s_tile;
-    const uint64_t r0 = (uint64_t)tile * kLongTile;
-    if (r0 >= U) break;
-    const uint64_t rt = r0 + (uint64_t)threadIdx.x * kLongItems;
-    uint32_t n_long = 0, n_items = 0, n_slots = 0;
-    uint32_t parts[kLongItems];
-#pragma unroll
-    for (int k = 0; k < kLongItems; ++k) {
-      parts[k] = 0;
-      const uint64_t r = rt + k;
-      if (r < U) {
-        const uint32_t SL = a.run_start[r + 1] - a.run_start[r];
-        if (SL >= a.thr) {
-          parts[k] = (SL + a.part - 1) / a.part;
-          n_long += 1;
-          n_items += parts[k];
-          if (parts[k] > 1) n_slots += parts[k];
-        }
-      }
-    }
-    uint32_t t_long, t_items, t_slots;
-    const uint32_t e_long = block_excl_scan(n_long, s_scan, &t_long);
-    const uint32_t e_items = block_excl_scan(n_items, s_scan, &t_items);
-    const uint32_t e_slots = block_excl_scan(n_slots, s_scan, &t_slots);
-    const uint32_t warp = threadIdx.x >> 5;
-    if (warp < 3) {  // one warp per channel
-      const uint32_t agg = warp == 0 ? t_long : (warp == 1 ? t_items : t_slots);
-      const uint32_t b = lookback_warp(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);
-      if ((threadIdx.x & 31) == 0) s_base[warp] = b;
-    }
-    __syncthreads();
-    uint32_t kl = s_base[0] + e_long, ki = s_base[1] + e_items, ks = s_base[2] + e_slots;
-    bool overflow = false;
-#pragma unroll
-    for (int k = 0; k < kLongItems; ++k) {
-      if (parts[k]) {
-        if (kl < a.cap_long && ki + parts[k] <= a.cap_items &&
-            (parts[k] == 1 || ks + parts[k] <= a.cap_slots)) {
-          a.long_ids[kl] = (uint32_t)(rt + k);
-          a.item_base[kl] = ki;
-          a.slot_base[kl] = ks;
-          for (uint32_t p = 0; p < parts[k]; ++p) a.item_long[ki + p] = kl;
+      const uint32_t SL = end - start;
+      if (SL >= a.thr) {
+        const uint32_t P = (SL + a.part - 1) / a.part;
+        if (kl < a.cap_long && ki + P <= a.cap_items && (P == 1 || ks + P <= a.cap_slots)) {
+          a.long_ids[kl] = r;
+          for (uint32_t q = 0; q < P; ++q) {
+            const uint32_t ps = start + q * a.part;
+            a.items[ki + q] = Item{ps, min(ps + a.part, end), key[k], P > 1 ? ks : 0u, q, P, 0u, 0u};
+          }
         } else {
           overflow = true;
         }
         kl += 1;
-        ki += parts[k];
-        if (parts[k] > 1) ks += parts[k];
+        ki += P;
+        if (P > 1) ks += P;
       }
+      ++r;
+      ++h;
     }
-    if (overflow) raise_error(a.ctl, a.sticky, kErrCapacity);
-    if (r0 + kLongTile >= U && threadIdx.x == 0) {
-      a.ctl->num_long = s_base[0] + t_long;
-      a.ctl->num_items = s_base[1] + t_items;
-      a.ctl->num_slots = s_base[2] + t_slots;
+  }
+  if (overflow) raise_error(a.ctl, a.sticky, kErrCapacity);
+  if (i0 + kRleTile >= N && threadIdx.x == 0) {  // the last tile knows every total
+    const uint32_t U = s_base[0] + n_heads;
+    if (U <= N) {
+      a.ctl->num_runs = U;
+      a.run_start[U] = N;
     }
-    __syncthreads();  // s_tile / s_base are rewritten by the next tile
+    a.ctl->num_long = s_base[1] + t_long;
+    a.ctl->num_items = s_base[2] + t_items;
+    a.ctl->num_slots = s_base[3] + t_slots;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_rle(const RleArgs& a, cudaStream_t s, bool pdl) {
+cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.N + kRleTile - 1) / kRleTile);
-  RleArgs arg = a;
+  RunsArgs arg = a;
   void* args[] = {&arg};
-  return launch_kernel(reinterpret_cast<const void*>(&k_rle), dim3(grid), dim3(kThreads), 0, s, args, pdl);
-}
-
-cudaError_t launch_long(const LongArgs& a, int grid, cudaStream_t s, bool pdl) {
-  LongArgs arg = a;
-  void* args[] = {&arg};
-  return launch_kernel(reinterpret_cast<const void*>(&k_long), dim3(grid), dim3(kThreads), 0, s, args, pdl);
+  return launch_kernel(reinterpret_cast<const void*>(&k_runs), dim3(grid), dim3(kThreads), 0, s,
+                       args, pdl);
 }
 
 }  // namespace embbwd

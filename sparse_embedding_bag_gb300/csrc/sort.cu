@@ -2,15 +2,15 @@
 // "fbgemm_gpu/codegen/embedding_backward_split_template.cu" (its host function
 // sorts linear_indices with their infos on bits [0, total_hash_size_bits)),
 // written as a one-sweep LSD radix sort for sm_103a:
-//   k_hist       one read of the indices: linearise, range-check, validate the
-//                CSR offsets, and histogram every pass's 8-bit digit;
+//   k_hist       one read of the indices: linearise each lookup to its 32-bit
+//                key hash_size_cumsum[t] + idx, range-check it, validate the
+//                CSR offsets, build the digit histograms of every pass, and
+//                write the (key, payload) pairs the passes sort;
 //   k_sort_pass  per pass: load a tile, rank it with warp match-based
 //                multisplit, publish/look back per-digit tile counts (decoupled
 //                look-back, bounded waits), scatter through shared memory so
 //                that global writes are runs of consecutive addresses.
-// The first pass rebuilds keys and payloads from the indices, so no key array
-// is ever materialised before sorting. The sort is stable: equal keys keep
-// lookup order.
+// The sort is stable: equal keys keep lookup order.
 #include "decode.cuh"
 
 namespace embbwd {
@@ -19,14 +19,18 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
-template <int ITEMS>
+// FIRST: the ValueKind of the payload to build, or -1 to only check (no pairs,
+// no histogram: the atomic path).
+template <int ITEMS, int FIRST>
 __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
   constexpr int TILE = kThreads * ITEMS;
+  using V = typename std::conditional<FIRST == VK_BAG_SCALED, uint64_t, uint32_t>::type;
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int HW = kMaxPasses * kRadix;                          // one warp's histograms
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem);           // [8 warps][passes][256]
   uint32_t* s_bag = s_hist + kWarps * HW;                          // [TILE]
-  uint32_t* s_hsc = s_bag + TILE;                                  // [T+1]
+  uint32_t* s_len = s_bag + TILE;                                  // [TILE]
+  uint32_t* s_hsc = s_len + TILE;                                  // [T+1]
   const DecodeArgs& d = a.d;
   pdl_wait();
   pdl_trigger();
@@ -43,48 +47,63 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
 
   const int64_t i0 = (int64_t)blockIdx.x * TILE;
   const int64_t i1 = min(i0 + TILE, d.N);
-  __syncthreads();
-  uint32_t bt_lo, bt_hi;
-  expand_tile_bags(d, i0, i1, s_bag, nullptr, reinterpret_cast<int64_t*>(s_hist), kWarps * HW / 2,
-                   &bt_lo, &bt_hi);
-  for (int i = threadIdx.x; i < kWarps * HW; i += kThreads) s_hist[i] = 0;
-  if (threadIdx.x == 0) {  // the first radix pass reuses the tile's bag range
-    a.tile_bags[2 * blockIdx.x] = bt_lo;
-    a.tile_bags[2 * blockIdx.x + 1] = bt_hi;
+  // the tile's indices (and per-sample weights) are independent of the bag search: load first
+  int64_t idx[ITEMS];
+  float psw[ITEMS];
+#pragma unroll
+  for (int k = 0; k < ITEMS; ++k) {
+    const int64_t pos = i0 + k * kThreads + threadIdx.x;
+    idx[k] = pos < i1 ? d.indices[pos] : 0;
+    if constexpr (FIRST == VK_BAG_SCALED) psw[k] = (pos < i1 && d.psw) ? d.psw[pos] : 1.0f;
   }
+  __syncthreads();
+  expand_tile_bags(d, i0, i1, s_bag, (FIRST == VK_BAG_SCALED && d.mean) ? s_len : nullptr,
+                   reinterpret_cast<int64_t*>(s_hist), kWarps * HW / 2);
+  for (int i = threadIdx.x; i < kWarps * HW; i += kThreads) s_hist[i] = 0;
   __syncthreads();
 
   // Per-warp private histograms in shared memory: plain shared atomics, no
   // contention between warps; colliding lanes of one warp are serialised.
   uint32_t* wh = s_hist + (threadIdx.x >> 5) * HW;
+  V* vals_out = reinterpret_cast<V*>(a.vals_out);
   bool any_bad = false;
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
     const int64_t pos = i0 + k * kThreads + threadIdx.x;
-    const bool valid = pos < i1;
-    uint32_t key = 0;
-    if (valid) {
-      uint32_t t;
-      bool bad;
-      key = linear_key(d, s_hsc, pos, s_bag[pos - i0], &t, &bad);
-      any_bad |= bad;
-    }
-    if (valid) {
-      for (int p = 0; p < a.passes; ++p) atomicAdd(&wh[p * kRadix + ((key >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+    if (pos < i1) {
+      const uint32_t bt = s_bag[pos - i0];
+      uint32_t t = div_by_B(bt, d.B, d.invB);
+      if (t >= d.T) t = d.T - 1;
+      const uint32_t base = s_hsc[t];
+      any_bad |= idx[k] < 0 || idx[k] >= (int64_t)(s_hsc[t + 1] - base);
+      const uint32_t key = base + (uint32_t)idx[k];
+      if constexpr (FIRST >= 0) {
+        for (int p = 0; p < a.passes; ++p) atomicAdd(&wh[p * kRadix + ((key >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+        a.keys_out[pos] = key;
+        if constexpr (FIRST == VK_BAG) {
+          vals_out[pos] = bt;
+        } else if constexpr (FIRST == VK_NOBAG) {
+          vals_out[pos] = (uint32_t)pos;
+        } else {
+          float s = psw[k];
+          if (d.mean) s = __fdiv_rn(s, (float)s_len[pos - i0]);
+          vals_out[pos] = (uint64_t)bt | ((uint64_t)__float_as_uint(s) << 32);
+        }
+      }
     }
   }
   if (__syncthreads_or(any_bad) && threadIdx.x == 0) raise_error(a.ctl, a.sticky, kErrIndex);
-  for (int i = threadIdx.x; i < a.passes * kRadix; i += kThreads) {
-    uint32_t c = 0;
+  if constexpr (FIRST >= 0) {
+    for (int i = threadIdx.x; i < a.passes * kRadix; i += kThreads) {
+      uint32_t c = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) c += s_hist[w * HW + i];
-    if (c) atomicAdd(&a.ctl->hist[0][0] + i, c);
+      for (int w = 0; w < kWarps; ++w) c += s_hist[w * HW + i];
+      if (c) atomicAdd(&a.ctl->hist[0][0] + i, c);
+    }
   }
 }
 
-// FIRST: -1 = keys/values from the previous pass; otherwise the ValueKind the
-// first pass builds from the indices.
-template <int ITEMS, int FIRST, typename V>
+template <int ITEMS, typename V>
 __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
   constexpr int TILE = kThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -94,31 +113,17 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
   uint32_t* s_misc = s_gbase + kRadix;                    // [16]
   uint32_t* s_keys = s_misc + 16;                         // [TILE]
   V* s_vals = reinterpret_cast<V*>(s_keys + TILE);        // [TILE]
-  uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_vals + TILE);  // [T+1] (first pass)
-  // The first pass's per-lookup bag ids (and bag lengths) alias the exchange buffers.
-  uint32_t* s_bag = s_keys;
-  uint32_t* s_len = reinterpret_cast<uint32_t*>(s_vals);
-  const DecodeArgs& d = a.d;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t N = a.N;
   pdl_wait();
   pdl_trigger();
 
   if (threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
-  if constexpr (FIRST < 0) {  // the first pass stages bag offsets in s_whist first
-    for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
-  }
-  if constexpr (FIRST >= 0) {
-    for (uint32_t i = threadIdx.x; i <= d.T; i += kThreads) s_hsc[i] = d.hsc[i];
-  }
+  for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
   __syncthreads();
   const uint32_t tile = s_misc[0];
   const int64_t i0 = (int64_t)tile * TILE;
-  const int64_t i1 = min(i0 + TILE, d.N);
-
-  if constexpr (FIRST >= 0)
-    expand_bag_range(d, i0, i1, a.tile_bags[2 * tile], a.tile_bags[2 * tile + 1], s_bag,
-                     (FIRST == VK_BAG_SCALED && d.mean) ? s_len : nullptr,
-                     reinterpret_cast<int64_t*>(s_whist), kWarps * kRadix / 2);
+  const int64_t i1 = min(i0 + TILE, N);
 
   uint32_t keys[ITEMS];
   V vals[ITEMS];
@@ -127,33 +132,8 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
 #pragma unroll
   for (int k = 0; k < ITEMS; ++k) {
     const int64_t pos = wbase + k * 32 + lane;
-    keys[k] = 0;
-    vals[k] = 0;
-    if (pos < i1) {
-      if constexpr (FIRST < 0) {
-        keys[k] = a.keys_in[pos];
-        vals[k] = reinterpret_cast<const V*>(a.vals_in)[pos];
-      } else {
-        const uint32_t bt = s_bag[pos - i0];
-        uint32_t t;
-        bool bad;
-        keys[k] = linear_key(d, s_hsc, pos, bt, &t, &bad);
-        if constexpr (FIRST == VK_BAG) {
-          vals[k] = (V)bt;
-        } else if constexpr (FIRST == VK_NOBAG) {
-          vals[k] = (V)pos;
-        } else {
-          float s = d.psw ? d.psw[pos] : 1.0f;
-          if (d.mean) s = __fdiv_rn(s, (float)s_len[pos - i0]);
-          vals[k] = (V)bt | ((V)__float_as_uint(s) << 32);
-        }
-      }
-    }
-  }
-  if constexpr (FIRST >= 0) {  // s_bag / s_len / staged offsets are dead from here on
-    __syncthreads();
-    for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
-    __syncthreads();
+    keys[k] = pos < i1 ? a.keys_in[pos] : 0u;
+    vals[k] = pos < i1 ? reinterpret_cast<const V*>(a.vals_in)[pos] : (V)0;
   }
 
   // Warp-level multisplit ranking: stable within the warp's slice of the tile.
@@ -211,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
     const uint32_t key = s_keys[q];
     const uint32_t digit = (key >> a.shift) & (kRadix - 1);
     const uint32_t out = s_gbase[digit] + q;
-    if (out < (uint64_t)d.N) {  // always true unless a look-back timed out
+    if (out < (uint64_t)N) {  // always true unless a look-back timed out
       a.keys_out[out] = key;
       vout[out] = s_vals[q];
     }
@@ -220,55 +200,44 @@ __global__ void __launch_bounds__(kThreads) k_sort_pass(PassArgs a) {
 
 template <int ITEMS>
 size_t hist_smem(int T) {
-  return (kWarps * kMaxPasses * kRadix + kThreads * ITEMS + T + 1) * sizeof(uint32_t);
+  return (kWarps * kMaxPasses * kRadix + 2 * kThreads * ITEMS + T + 1) * sizeof(uint32_t);
 }
 
 template <int ITEMS, typename V>
-size_t pass_smem(int T) {
+size_t pass_smem() {
   return (kWarps * kRadix + 2 * kRadix + 16) * sizeof(uint32_t) +
-         (size_t)kThreads * ITEMS * (sizeof(uint32_t) + sizeof(V)) + (T + 1) * sizeof(uint32_t);
+         (size_t)kThreads * ITEMS * (sizeof(uint32_t) + sizeof(V));
 }
 
-template <int ITEMS, int FIRST, typename V>
-cudaError_t set_pass_attr(int T) {
-  return cudaFuncSetAttribute(k_sort_pass<ITEMS, FIRST, V>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)pass_smem<ITEMS, V>(T));
+template <int ITEMS, int FIRST>
+cudaError_t set_hist_attr() {
+  return cudaFuncSetAttribute(k_hist<ITEMS, FIRST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)hist_smem<ITEMS>(kMaxT));
 }
 
 template <int ITEMS>
-cudaError_t configure_items(int T) {
-  cudaError_t e = cudaFuncSetAttribute(k_hist<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)hist_smem<ITEMS>(T));
-  if (e == cudaSuccess) e = set_pass_attr<ITEMS, -1, uint32_t>(T);
-  if (e == cudaSuccess) e = set_pass_attr<ITEMS, -1, uint64_t>(T);
-  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_BAG, uint32_t>(T);
-  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_NOBAG, uint32_t>(T);
-  if (e == cudaSuccess) e = set_pass_attr<ITEMS, VK_BAG_SCALED, uint64_t>(T);
+cudaError_t configure_items() {
+  cudaError_t e = set_hist_attr<ITEMS, -1>();
+  if (e == cudaSuccess) e = set_hist_attr<ITEMS, VK_BAG>();
+  if (e == cudaSuccess) e = set_hist_attr<ITEMS, VK_BAG_SCALED>();
+  if (e == cudaSuccess) e = set_hist_attr<ITEMS, VK_NOBAG>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_sort_pass<ITEMS, uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pass_smem<ITEMS, uint32_t>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_sort_pass<ITEMS, uint64_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pass_smem<ITEMS, uint64_t>());
   return e;
 }
 
-template <int ITEMS, typename V>
-cudaError_t launch_pass_items(const PassArgs& a, int first_kind, int T, cudaStream_t s, bool pdl) {
-  const unsigned grid = (unsigned)((a.d.N + kThreads * ITEMS - 1) / (kThreads * ITEMS));
-  PassArgs arg = a;
-  void* args[] = {&arg};
-  const void* fn;
-  size_t sm;
-  if (first_kind < 0) {
-    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, -1, V>);
-    sm = pass_smem<ITEMS, V>(T);
-  } else if (first_kind == VK_BAG_SCALED) {
-    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_BAG_SCALED, uint64_t>);
-    sm = pass_smem<ITEMS, uint64_t>(T);
-  } else if (first_kind == VK_BAG) {
-    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_BAG, uint32_t>);
-    sm = pass_smem<ITEMS, uint32_t>(T);
-  } else {
-    fn = reinterpret_cast<const void*>(&k_sort_pass<ITEMS, VK_NOBAG, uint32_t>);
-    sm = pass_smem<ITEMS, uint32_t>(T);
+template <int ITEMS>
+const void* hist_fn(int first_kind) {
+  switch (first_kind) {
+    case VK_BAG: return reinterpret_cast<const void*>(&k_hist<ITEMS, VK_BAG>);
+    case VK_BAG_SCALED: return reinterpret_cast<const void*>(&k_hist<ITEMS, VK_BAG_SCALED>);
+    case VK_NOBAG: return reinterpret_cast<const void*>(&k_hist<ITEMS, VK_NOBAG>);
+    default: return reinterpret_cast<const void*>(&k_hist<ITEMS, -1>);
   }
-  return launch_kernel(fn, dim3(grid), dim3(kThreads), sm, s, args, pdl);
 }
 
 }  // namespace
@@ -277,38 +246,38 @@ cudaError_t launch_pass_items(const PassArgs& a, int first_kind, int T, cudaStre
 // tiles cut look-back traffic on large ones.
 size_t sort_tile_for(int64_t N) { return N <= (int64_t)(1 << 21) ? kThreads * 4 : kThreads * 16; }
 
-size_t sort_smem_bytes(int tile, bool wide_vals, bool first, int T) {
-  (void)first;
-  if (tile == kThreads * 4) return wide_vals ? pass_smem<4, uint64_t>(T) : pass_smem<4, uint32_t>(T);
-  return wide_vals ? pass_smem<16, uint64_t>(T) : pass_smem<16, uint32_t>(T);
-}
-
 cudaError_t sort_configure(const DevProps& p) {
   (void)p;
-  cudaError_t e = configure_items<4>(kMaxT);
-  if (e == cudaSuccess) e = configure_items<16>(kMaxT);
+  cudaError_t e = configure_items<4>();
+  if (e == cudaSuccess) e = configure_items<16>();
   return e;
 }
 
-cudaError_t launch_hist(const HistArgs& a, int T, cudaStream_t s, bool pdl) {
+cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.d.N + a.tile - 1) / a.tile);
   HistArgs arg = a;
   void* args[] = {&arg};
   if (a.tile == kThreads * 4)
-    return launch_kernel(reinterpret_cast<const void*>(&k_hist<4>), dim3(grid), dim3(kThreads),
-                         hist_smem<4>(T), s, args, pdl);
-  return launch_kernel(reinterpret_cast<const void*>(&k_hist<16>), dim3(grid), dim3(kThreads),
-                       hist_smem<16>(T), s, args, pdl);
+    return launch_kernel(hist_fn<4>(first_kind), dim3(grid), dim3(kThreads), hist_smem<4>(T), s, args, pdl);
+  return launch_kernel(hist_fn<16>(first_kind), dim3(grid), dim3(kThreads), hist_smem<16>(T), s, args, pdl);
 }
 
-cudaError_t launch_sort_pass(const PassArgs& a, int first_kind, bool wide_vals, int tile, int T,
-                             cudaStream_t s, bool pdl) {
+cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl) {
+  const unsigned grid = (unsigned)((a.N + tile - 1) / tile);
+  PassArgs arg = a;
+  void* args[] = {&arg};
+  const void* fn;
+  size_t sm;
   if (tile == kThreads * 4) {
-    return wide_vals ? launch_pass_items<4, uint64_t>(a, first_kind, T, s, pdl)
-                     : launch_pass_items<4, uint32_t>(a, first_kind, T, s, pdl);
+    fn = wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<4, uint64_t>)
+                   : reinterpret_cast<const void*>(&k_sort_pass<4, uint32_t>);
+    sm = wide_vals ? pass_smem<4, uint64_t>() : pass_smem<4, uint32_t>();
+  } else {
+    fn = wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<16, uint64_t>)
+                   : reinterpret_cast<const void*>(&k_sort_pass<16, uint32_t>);
+    sm = wide_vals ? pass_smem<16, uint64_t>() : pass_smem<16, uint32_t>();
   }
-  return wide_vals ? launch_pass_items<16, uint64_t>(a, first_kind, T, s, pdl)
-                   : launch_pass_items<16, uint32_t>(a, first_kind, T, s, pdl);
+  return launch_kernel(fn, dim3(grid), dim3(kThreads), sm, s, args, pdl);
 }
 
 }  // namespace embbwd
