@@ -322,9 +322,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   const int nvec = max_D / 4;
   p->kv = nvec <= 32 ? 1 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
   p->C = (uint32_t)((nvec + p->kv * 32 - 1) / (p->kv * 32));
-  // Short runs: teams of lanes as wide as the widest row (in 16-byte vectors, at most a warp).
+  // Short runs: teams of lanes as wide as the widest row's lane group (each lane holds kv
+  // vectors of a row; at most a warp).
+  const int per_lane = (std::min(nvec, p->kv * 32) + p->kv - 1) / p->kv;
   p->team_log2 = 0;
-  while ((1 << p->team_log2) < std::min(nvec, 32)) ++p->team_log2;
+  while ((1 << p->team_log2) < per_lane) ++p->team_log2;
   // Long runs: parts of about 64 KB of gradient reads (one row chunk per lookup).
   const uint32_t chunk_bytes = (uint32_t)std::min(max_D, p->kv * 128) * (grad_dtype == EMB_F32 ? 4u : 2u);
   p->base_part = std::min(kMaxPart, std::max(kMinPart, pow2floor(65536 / chunk_bytes)));

@@ -74,7 +74,7 @@ struct RowShape {
 // Lookups gathered per lane group and step, unrolled for memory-level parallelism.
 template <int KV>
 struct Unroll {
-  static constexpr int value = KV >= 8 ? 2 : (KV >= 4 ? 1 : 4 / KV);
+  static constexpr int value = KV >= 4 ? 2 : 4;
 };
 
 // Minimum resident blocks per SM, by vectors per lane (register budget).
@@ -95,8 +95,23 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
   using V = typename ValT<VK>::type;
   constexpr int UNR = Unroll<KV>::value;
   const V* vals = reinterpret_cast<const V*>(a.vals);
-  const grad_t* grad = static_cast<const grad_t*>(a.grad);
-  const uint32_t Lg = 1u << rs.lg;
+  // Byte address of gradient row 0 of this run's table chunk; a lookup adds
+  // (bag or lookup id) * stride with one 32x32->64 multiply. For pooled rows the
+  // bag id's table part t*B is folded into the base (kept as an integer).
+  const uint64_t stride = (uint64_t)a.grad_stride * sizeof(grad_t);
+  // (unpooled gradient rows are [N, D]: no table column offset)
+  const uint64_t goff = VK == VK_NOBAG ? 0ull : (uint64_t)rs.goff;
+  uint64_t base = reinterpret_cast<uint64_t>(a.grad) + (goff + rs.cvec_off * 4ull) * sizeof(grad_t);
+  if constexpr (VK != VK_NOBAG) base -= (uint64_t)(rs.t * a.B) * stride;
+  // per-lane columns and masks of the chunk, the same for every lookup
+  uint32_t col[KV];
+  bool on[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const uint32_t q = li + (k << rs.lg);
+    on[k] = q < rs.cvec;
+    col[k] = q * 4 * (uint32_t)sizeof(grad_t);
+  }
 #pragma unroll
   for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (uint32_t s = 0; s < steps; ++s) {
@@ -112,21 +127,13 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
     float scale[UNR];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
-      const grad_t* row;
+      const uint64_t row = base + (uint64_t)(uint32_t)v[u] * stride;
       scale[u] = 1.0f;
-      if constexpr (VK == VK_NOBAG) {
-        row = grad + (int64_t)(uint32_t)v[u] * a.grad_stride;
-      } else {
-        const uint32_t b = (uint32_t)v[u] - rs.t * a.B;
-        row = grad + (int64_t)b * a.grad_stride + rs.goff;
-        if constexpr (VK == VK_BAG_SCALED) scale[u] = __uint_as_float((uint32_t)(v[u] >> 32));
-      }
+      if constexpr (VK == VK_BAG_SCALED) scale[u] = __uint_as_float((uint32_t)(v[u] >> 32));
 #pragma unroll
-      for (int k = 0; k < KV; ++k) {
-        const uint32_t q = li + k * Lg;
-        x[u][k] = (ok[u] && q < rs.cvec) ? Vec4<grad_t>::load(row + (int64_t)(rs.cvec_off + q) * 4)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int k = 0; k < KV; ++k)
+        x[u][k] = (ok[u] && on[k]) ? Vec4<grad_t>::load(reinterpret_cast<const grad_t*>(row + col[k]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -216,7 +223,9 @@ __device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* 
   const uint32_t nvec = rs->D >> 2;
   rs->cvec_off = c * (KV * 32);
   rs->cvec = rs->cvec_off < nvec ? min((uint32_t)(KV * 32), nvec - rs->cvec_off) : 0u;
-  rs->lg = log2_pow2ceil32(rs->cvec);
+  // lanes per lookup: the row's vectors spread so that each lane holds KV of them
+  const uint32_t per_lane = (rs->cvec + KV - 1) / KV;
+  rs->lg = log2_pow2ceil32(per_lane);
   return rs->cvec != 0;
 }
 
