@@ -320,7 +320,12 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->max_D = max_D;
   p->uniform_D = uniform;
   const int nvec = max_D / 4;
-  p->kv = nvec <= 32 ? 1 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
+  // 16-byte vectors each lane holds of a row (rows wider than kv*32 vectors are cut
+  // into chunks). Narrow rows take more than they need, so that a row spans only a
+  // few lanes and a warp works on several short runs at once (the short runs of
+  // skewed batches are mostly single lookups); measured on GB300, kv = 8 costs too
+  // much occupancy, so rows of 33-64 vectors stay at kv = 2.
+  p->kv = nvec <= 8 ? 1 : nvec <= 16 ? 2 : nvec <= 32 ? 4 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
   p->C = (uint32_t)((nvec + p->kv * 32 - 1) / (p->kv * 32));
   // Short runs: teams of lanes as wide as the widest row's lane group (each lane holds kv
   // vectors of a row; at most a warp).

@@ -13,7 +13,8 @@ import threading
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libembbwd.so")
+# EMBBWD_LIB selects another build of the library (e.g. for side-by-side timing).
+LIB_PATH = os.environ.get("EMBBWD_LIB") or os.path.join(_PKG, "libembbwd.so")
 
 EMB_OK, EMB_ERR_INVALID_ARG, EMB_ERR_UNSUPPORTED, EMB_ERR_INDEX_OUT_OF_RANGE = 0, 1, 2, 3
 EMB_ERR_OOM, EMB_ERR_CUDA, EMB_ERR_TIMEOUT = 4, 5, 6
