@@ -54,11 +54,14 @@ struct emb_plan {
   uint32_t flags = 0;
   int max_D = 0;
   bool uniform_D = true;
-  int kv = 1;
-  uint32_t C = 1;
+  // How the reduce splits rows, per optimizer (0 SGD, 1 row-wise Adagrad).
+  struct RowSplit {
+    int kv = 1;                     // 16-byte vectors per lane
+    uint32_t C = 1;                 // chunks of kv*32 vectors per row
+    uint32_t team_log2 = 5;         // lanes per short-run team
+    uint32_t base_part = kMaxPart;  // lookups per long-run work item (before batch scaling)
+  } split[2];
   int key_bits = 1;
-  uint32_t team_log2 = 5;
-  uint32_t base_part = kMaxPart;
   std::vector<uint32_t> hsc;
   std::vector<int32_t> Do;
   DevProps props{};
@@ -96,7 +99,7 @@ struct emb_plan {
 namespace {
 
 const void* reduce_fn(const emb_plan* p, int opt, int vk) {
-  ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->kv};
+  ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->split[opt].kv};
   switch (p->wdt) {
     case EMB_F32: return reduce_kernel_f32(k);
     case EMB_F16: return reduce_kernel_f16(k);
@@ -117,9 +120,9 @@ emb_status record(emb_plan* p, int i, cudaStream_t s) {
 // Lookups per block work item of a long run: about 64 KB of gradient reads
 // (base_part), raised for large batches so that there are a few items per
 // resident warp rather than many tiny ones.
-uint32_t part_for(const emb_plan* p, int64_t N) {
+uint32_t part_for(const emb_plan* p, int opt, int64_t N) {
   const uint32_t by_n = pow2floor((uint64_t)N / (32ull * p->props.sms));
-  return std::min(kMaxPart, std::max(p->base_part, by_n));
+  return std::min(kMaxPart, std::max(p->split[opt].base_part, by_n));
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -215,7 +218,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.run_key = p->run_key;
   ra.run_start = p->run_start;
   ra.thr = p->thr;
-  ra.part = part_for(p, N);
+  ra.part = part_for(p, opt, N);
   ra.long_ids = p->long_ids;
   ra.items = p->items;
   ra.cap_long = p->cap_long;
@@ -247,13 +250,13 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.eps = eps;
   r.thr = p->thr;
   r.part = ra.part;
-  r.C = p->C;
-  r.team_log2 = p->team_log2;
+  r.C = p->split[opt].C;
+  r.team_log2 = p->split[opt].team_log2;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
   EMB_CUDA(launch_kernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads),
-                         reduce_smem_bytes(p->kv, p->T), s, args, pdl));
+                         reduce_smem_bytes(p->split[opt].kv, p->T), s, args, pdl));
   EMB_TRY(record(p, 5, s));
   p->last_kind = 1;
   p->last_N = N;
@@ -320,21 +323,27 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->max_D = max_D;
   p->uniform_D = uniform;
   const int nvec = max_D / 4;
-  // 16-byte vectors each lane holds of a row (rows wider than kv*32 vectors are cut
-  // into chunks). Narrow rows take more than they need, so that a row spans only a
-  // few lanes and a warp works on several short runs at once (the short runs of
-  // skewed batches are mostly single lookups); measured on GB300, kv = 8 costs too
-  // much occupancy, so rows of 33-64 vectors stay at kv = 2.
-  p->kv = nvec <= 8 ? 1 : nvec <= 16 ? 2 : nvec <= 32 ? 4 : nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8;
-  p->C = (uint32_t)((nvec + p->kv * 32 - 1) / (p->kv * 32));
-  // Short runs: teams of lanes as wide as the widest row's lane group (each lane holds kv
-  // vectors of a row; at most a warp).
-  const int per_lane = (std::min(nvec, p->kv * 32) + p->kv - 1) / p->kv;
-  p->team_log2 = 0;
-  while ((1 << p->team_log2) < per_lane) ++p->team_log2;
-  // Long runs: parts of about 64 KB of gradient reads (one row chunk per lookup).
-  const uint32_t chunk_bytes = (uint32_t)std::min(max_D, p->kv * 128) * (grad_dtype == EMB_F32 ? 4u : 2u);
-  p->base_part = std::min(kMaxPart, std::max(kMinPart, pow2floor(65536 / chunk_bytes)));
+  for (int opt = 0; opt < 2; ++opt) {
+    emb_plan::RowSplit& sp = p->split[opt];
+    // 16-byte vectors each lane holds of a row (rows wider than kv*32 vectors are
+    // cut into chunks). Narrow rows take more than they need, so that a row spans
+    // only a few lanes and a warp works on several short runs at once (the short
+    // runs of skewed batches are mostly single lookups). Measured on GB300: kv = 8
+    // costs too much occupancy, so rows of 33-64 vectors stay at kv = 2, and SGD
+    // cuts rows wider than 64 vectors into chunks of 64 (kv = 2). Row-wise Adagrad
+    // needs the whole row in one warp for its norm, so it widens kv instead.
+    if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 16 ? 2 : nvec <= 32 ? 4 : 2;
+    else sp.kv = opt == 0 ? 2 : nvec <= 128 ? 4 : 8;
+    sp.C = (uint32_t)((nvec + sp.kv * 32 - 1) / (sp.kv * 32));
+    // Short runs: teams of lanes as wide as the widest row's lane group (each lane
+    // holds kv vectors of a row; at most a warp).
+    const int per_lane = (std::min(nvec, sp.kv * 32) + sp.kv - 1) / sp.kv;
+    sp.team_log2 = 0;
+    while ((1 << sp.team_log2) < per_lane) ++sp.team_log2;
+    // Long runs: parts of about 64 KB of gradient reads (one row chunk per lookup).
+    const uint32_t chunk_bytes = (uint32_t)std::min(max_D, sp.kv * 128) * (grad_dtype == EMB_F32 ? 4u : 2u);
+    sp.base_part = std::min(kMaxPart, std::max(kMinPart, pow2floor(65536 / chunk_bytes)));
+  }
   const uint64_t total_rows = (uint64_t)hash_size_cumsum[T];
   p->key_bits = 1;
   while (p->key_bits < 32 && ((uint64_t)1 << p->key_bits) < total_rows) ++p->key_bits;
@@ -365,7 +374,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->cap_long = (uint32_t)(N / p->thr + 1);
   p->cap_items = (uint32_t)std::min<uint64_t>(parts_bound + p->cap_long, N + 1);
   p->cap_slots = (uint32_t)(2 * parts_bound + 2);
-  const size_t part_row = (size_t)p->kv * 32 * sizeof(float4);
+  // fp32 partial rows of long-run parts: one chunk of kv*32 vectors per slot and chunk
+  size_t part_bytes = 0;
+  for (const emb_plan::RowSplit& sp : p->split)
+    part_bytes = std::max(part_bytes, (size_t)sp.C * sp.kv * 32 * sizeof(float4));
+  const uint32_t max_C = std::max(p->split[0].C, p->split[1].C);
   struct Seg {
     void** ptr;
     size_t bytes;
@@ -389,8 +402,8 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->items), p->cap_items * sizeof(Item)},
-      {reinterpret_cast<void**>(&p->partials), (size_t)p->cap_slots * p->C * part_row},
-      {reinterpret_cast<void**>(&p->done), (size_t)p->cap_slots * p->C * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->partials), (size_t)p->cap_slots * part_bytes},
+      {reinterpret_cast<void**>(&p->done), (size_t)p->cap_slots * max_C * sizeof(uint32_t)},
   };
   size_t total = 0;
   for (const Seg& sg : segs) total = align_up(total, 256) + sg.bytes;
@@ -421,7 +434,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     for (int vk = 0; vk < 3 && e == cudaSuccess; ++vk) {
       const void* fn = reduce_fn(p, opt, vk);
       if (!fn) continue;
-      const size_t sm = reduce_smem_bytes(p->kv, T);
+      const size_t sm = reduce_smem_bytes(p->split[opt].kv, T);
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       int blocks = 0;
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm);
@@ -475,7 +488,7 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* moment
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
-  if (p->C != 1) return EMB_ERR_UNSUPPORTED;  // the row-wise norm needs the whole row in one warp
+  if (p->split[1].C != 1) return EMB_ERR_UNSUPPORTED;  // the row-wise norm needs the whole row in one warp
   if (N == 0) {
     p->last_kind = 0;
     return EMB_OK;

@@ -171,6 +171,17 @@ def test_tile_boundaries_ragged_tail():
         run_and_check(w)
 
 
+@pytest.mark.parametrize("rows", [[32], [600], [3000], [300_000], [150_000, 150_000], [(1 << 20) + 5],
+                                  [(1 << 24) + 3]])
+def test_key_widths(rows):
+    # total rows fix the key width: 5 to 25 bits, sorted in 1 to 4 radix passes
+    def ids(r, t, n):  # half hot (Zipf), half uniform so that every digit varies
+        return np.where(r.random(n) < 0.5, synth.sample_zipf(r, rows[t], 1.05, n), r.integers(0, rows[t], n))
+
+    w = custom(17 + rows[0], rows, [4] * len(rows), 600, lambda r, T, B: r.integers(0, 20, (T, B)), ids_fn=ids)
+    run_and_check(w)
+
+
 def test_large_batch_uses_big_tiles():
     # > 2^21 lookups selects the 4096-lookup sort tiles
     w = custom(15, [50_000, 200_000], [16, 32], 40_000, lambda r, T, B: r.integers(20, 40, (T, B)),
