@@ -91,7 +91,8 @@ typedef struct emb_plan emb_plan;
  *   momentum_offsets  host int64[T] or NULL.
  *   weight_dtype      storage type of weights (fp32, fp16, bf16).
  *   grad_dtype        type of grad_output (fp32, fp16, bf16).
- *   max_N             largest lookup count any call will pass (< 2^30).
+ *   max_N             largest lookup count any call will pass (< 2^30, and
+ *                     max_N * ceil(max D_t / 256) < 2^31).
  *   max_B             largest batch any call will pass (max_B * T < 2^31).
  *   max_segment_length_per_warp  runs at least this long take the block-level
  *                     path ("embedding_backward_split_template.cu",

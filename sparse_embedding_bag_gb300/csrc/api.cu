@@ -18,8 +18,7 @@ using namespace embbwd;
 namespace {
 
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls before a look-back wait gives up (~1 s)
-constexpr uint32_t kMaxPart = 1024;        // lookups per block work item of a long run, at most
-constexpr uint32_t kMinPart = 32;
+constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups per reduce warp slice
 constexpr int kStages = 5;
 
 struct DeviceGuard {
@@ -59,7 +58,6 @@ struct emb_plan {
     int kv = 1;                     // 16-byte vectors per lane
     uint32_t C = 1;                 // chunks of kv*32 vectors per row
     uint32_t team_log2 = 5;         // lanes per short-run team
-    uint32_t base_part = kMaxPart;  // lookups per long-run work item (before batch scaling)
   } split[2];
   int key_bits = 1;
   std::vector<uint32_t> hsc;
@@ -79,10 +77,10 @@ struct emb_plan {
   uint32_t* run_key = nullptr;
   uint32_t* run_start = nullptr;
   uint32_t* long_ids = nullptr;
-  Item* items = nullptr;
+  LongRun* longs = nullptr;
   float4* partials = nullptr;
   uint32_t* done = nullptr;
-  uint32_t cap_long = 0, cap_items = 0, cap_slots = 0;
+  uint32_t cap_long = 0, cap_slices = 0;
 
   uint32_t seq = 0;
   int reduce_grid[2][3] = {{0, 0, 0}, {0, 0, 0}};
@@ -115,14 +113,6 @@ emb_status record(emb_plan* p, int i, cudaStream_t s) {
                             ? cudaEventRecordWithFlags(p->ev[i], s, cudaEventRecordExternal)
                             : cudaEventRecord(p->ev[i], s);
   return e == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
-}
-
-// Lookups per block work item of a long run: about 64 KB of gradient reads
-// (base_part), raised for large batches so that there are a few items per
-// resident warp rather than many tiny ones.
-uint32_t part_for(const emb_plan* p, int opt, int64_t N) {
-  const uint32_t by_n = pow2floor((uint64_t)N / (32ull * p->props.sms));
-  return std::min(kMaxPart, std::max(p->split[opt].base_part, by_n));
 }
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -218,12 +208,9 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.run_key = p->run_key;
   ra.run_start = p->run_start;
   ra.thr = p->thr;
-  ra.part = part_for(p, opt, N);
   ra.long_ids = p->long_ids;
-  ra.items = p->items;
+  ra.longs = p->longs;
   ra.cap_long = p->cap_long;
-  ra.cap_items = p->cap_items;
-  ra.cap_slots = p->cap_slots;
   EMB_CUDA(launch_runs(ra, s, pdl));
   EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel
   EMB_TRY(record(p, 4, s));
@@ -233,9 +220,10 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.vals = static_cast<const uint32_t*>(p->vals[fin]);
   r.run_key = p->run_key;
   r.run_start = p->run_start;
-  r.items = p->items;
+  r.longs = p->longs;
   r.partials = p->partials;
   r.done = p->done;
+  r.done_run = p->done + 2 * (size_t)p->cap_slices;
   r.grad = grad;
   r.weights = weights;
   r.momentum = momentum;
@@ -249,14 +237,14 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.lr = lr;
   r.eps = eps;
   r.thr = p->thr;
-  r.part = ra.part;
+  r.min_slice = kMinSlice;
   r.C = p->split[opt].C;
   r.team_log2 = p->split[opt].team_log2;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
   EMB_CUDA(launch_kernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads),
-                         reduce_smem_bytes(p->split[opt].kv, p->T), s, args, pdl));
+                         reduce_smem_bytes(p->T), s, args, pdl));
   EMB_TRY(record(p, 5, s));
   p->last_kind = 1;
   p->last_N = N;
@@ -340,9 +328,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     const int per_lane = (std::min(nvec, sp.kv * 32) + sp.kv - 1) / sp.kv;
     sp.team_log2 = 0;
     while ((1 << sp.team_log2) < per_lane) ++sp.team_log2;
-    // Long runs: parts of about 64 KB of gradient reads (one row chunk per lookup).
-    const uint32_t chunk_bytes = (uint32_t)std::min(max_D, sp.kv * 128) * (grad_dtype == EMB_F32 ? 4u : 2u);
-    sp.base_part = std::min(kMaxPart, std::max(kMinPart, pow2floor(65536 / chunk_bytes)));
+  }
+  // the reduce counts (run x row chunk) tasks in 32 bits, with headroom
+  if ((uint64_t)std::max<int64_t>(max_N, 1) * std::max(p->split[0].C, p->split[1].C) >= (1ull << 31)) {
+    delete p;
+    return EMB_ERR_INVALID_ARG;
   }
   const uint64_t total_rows = (uint64_t)hash_size_cumsum[T];
   p->key_bits = 1;
@@ -364,21 +354,44 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->props.sms = prop.multiProcessorCount;
   p->props.smem_optin = (int)prop.sharedMemPerBlockOptin;
 
+  // Reduce kernels of this plan's types: shared-memory limit and persistent grid.
+  int max_grid = 1;
+  {
+    cudaError_t e = cudaSuccess;
+    for (int opt = 0; opt < 2 && e == cudaSuccess; ++opt) {
+      for (int vk = 0; vk < 3 && e == cudaSuccess; ++vk) {
+        const void* fn = reduce_fn(p, opt, vk);
+        if (!fn) continue;
+        const size_t sm = reduce_smem_bytes(T);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        int blocks = 0;
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm);
+        p->reduce_grid[opt][vk] = std::max(blocks, 1) * p->props.sms;
+        max_grid = std::max(max_grid, p->reduce_grid[opt][vk]);
+      }
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return EMB_ERR_CUDA;
+    }
+  }
+
   // ---- scratch sizes
   const uint64_t N = (uint64_t)std::max<int64_t>(max_N, 1);
   const uint64_t sort_tiles = std::max<uint64_t>((N + 1023) / 1024, 1);  // smallest tile is 1024
   const uint64_t status_words = std::max<uint64_t>(sort_tiles * kRadix, (N + kRleTile - 1) / kRleTile * 4);
-  // part_for(N) >= N / (2 * sms * 32) and >= base_part, so no call has more than
-  // max(N / kMaxPart, 2 * sms * 32) long-run parts beyond one per long run.
-  const uint64_t parts_bound = std::max<uint64_t>(N / kMaxPart + 1, 2ull * p->props.sms * 32 + 1);
   p->cap_long = (uint32_t)(N / p->thr + 1);
-  p->cap_items = (uint32_t)std::min<uint64_t>(parts_bound + p->cap_long, N + 1);
-  p->cap_slots = (uint32_t)(2 * parts_bound + 2);
-  // fp32 partial rows of long-run parts: one chunk of kv*32 vectors per slot and chunk
-  size_t part_bytes = 0;
-  for (const emb_plan::RowSplit& sp : p->split)
-    part_bytes = std::max(part_bytes, (size_t)sp.C * sp.kv * 32 * sizeof(float4));
-  const uint32_t max_C = std::max(p->split[0].C, p->split[1].C);
+  // Slices (row chunk x slice) the reduce cuts the long runs into: at most
+  // warps + C with one slice per warp; with more, at most 44 * warps + C and at
+  // most C * (N / kMinSlice + 2). Each has a head and a tail partial row of kv*32
+  // vectors.
+  {
+    const uint64_t warps = (uint64_t)max_grid * kWarps;
+    const uint64_t C = std::max(p->split[0].C, p->split[1].C);
+    p->cap_slices = (uint32_t)(warps + C + std::min<uint64_t>(48 * warps, C * (N / kMinSlice + 2)));
+  }
+  const size_t part_row = (size_t)std::max(p->split[0].kv, p->split[1].kv) * 32 * sizeof(float4);
   struct Seg {
     void** ptr;
     size_t bytes;
@@ -401,9 +414,9 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {reinterpret_cast<void**>(&p->run_key), N * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
-      {reinterpret_cast<void**>(&p->items), p->cap_items * sizeof(Item)},
-      {reinterpret_cast<void**>(&p->partials), (size_t)p->cap_slots * part_bytes},
-      {reinterpret_cast<void**>(&p->done), (size_t)p->cap_slots * max_C * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->longs), p->cap_long * sizeof(LongRun)},
+      {reinterpret_cast<void**>(&p->partials), 2 * (size_t)p->cap_slices * part_row},
+      {reinterpret_cast<void**>(&p->done), 4 * (size_t)p->cap_slices * sizeof(uint32_t)},
   };
   size_t total = 0;
   for (const Seg& sg : segs) total = align_up(total, 256) + sg.bytes;
@@ -429,18 +442,6 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   if (e == cudaSuccess) e = cudaMemcpy(p->d_wo, weights_offsets, T * sizeof(int64_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_mo, mo.data(), T * sizeof(int64_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = sort_configure(p->props);
-  // Reduce kernels of this plan's types: shared-memory limit and persistent grid.
-  for (int opt = 0; opt < 2 && e == cudaSuccess; ++opt) {
-    for (int vk = 0; vk < 3 && e == cudaSuccess; ++vk) {
-      const void* fn = reduce_fn(p, opt, vk);
-      if (!fn) continue;
-      const size_t sm = reduce_smem_bytes(p->split[opt].kv, T);
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      int blocks = 0;
-      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm);
-      p->reduce_grid[opt][vk] = std::max(blocks, 1) * p->props.sms;
-    }
-  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     cudaFree(p->arena);

@@ -10,12 +10,13 @@
 //               reading a materialised key array.
 //   k_runs      run-length encode of the sorted keys (unique keys, run starts,
 //               number of runs) fused with the ordered compaction of runs with
-//               >= max_segment_length_per_warp lookups into block work items
-//               (hot rows split into parts); one pass, decoupled look-back.
-//   k_reduce    persistent: block-level work items for long runs (multi-block
-//               parts combined in a fixed order), then one warp per short run;
-//               fp32 accumulation of the scaled gradient rows and the optimizer
-//               update fused in the same kernel.
+//               >= max_segment_length_per_warp lookups (with the prefix sum of
+//               their lengths); one pass, decoupled look-back.
+//   k_reduce    persistent: every warp first reduces an equal slice of the
+//               concatenated long runs (runs cut by slice ends are combined from
+//               fp32 partials in a fixed order), then strides over the short
+//               runs in lane teams; fp32 accumulation of the scaled gradient rows
+//               and the optimizer update fused in the same kernel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -34,8 +35,6 @@ constexpr int kRadix = 1 << kRadixBits;
 constexpr int kMaxPasses = 4;  // 32-bit keys
 constexpr int kRleItems = 8;
 constexpr int kRleTile = kThreads * kRleItems;
-constexpr int kLongItems = 4;
-constexpr int kLongTile = kThreads * kLongItems;
 constexpr int kMaxT = 4096;
 
 // Device-side error bits (per call in Ctl::err, accumulated in the plan's sticky word).
@@ -53,11 +52,12 @@ struct Ctl {
   uint32_t tile_ctr[TC_COUNT];
   uint32_t num_runs;
   uint32_t num_long;
-  uint32_t num_items;
-  uint32_t num_slots;
-  uint32_t item_ctr;
-  uint32_t pad[2];
+  uint32_t long_lookups;  // lookups in long runs
+  uint32_t pad[4];
   uint32_t hist[kMaxPasses][kRadix];
+  // Reduce: long-run slices handed out dynamically, one counter per warp index
+  // of a block (each in its own 128-byte line).
+  uint32_t slice_ctr[kWarps][32];
 };
 
 // Sort-value kinds: what travels with each key through the radix passes.
@@ -114,10 +114,11 @@ struct PassArgs {
   int shift;
 };
 
-// One block work item of a long run: lookups [ps, pe) of the run with linear
-// index `key`; part q of P. Runs with P > 1 own partial-sum slots slot0 .. slot0+P-1.
-struct __align__(16) Item {
-  uint32_t ps, pe, key, slot0, q, P, pad0, pad1;
+// A long run: sorted lookups [start, start + len) of linear index `key`;
+// lpos = lookups in the long runs before it (its place in the concatenation of
+// all long runs, which the reduce cuts into equal slices).
+struct __align__(16) LongRun {
+  uint32_t start, len, key, lpos;
 };
 
 struct RunsArgs {
@@ -129,10 +130,9 @@ struct RunsArgs {
   uint32_t* run_key;
   uint32_t* run_start;   // [U+1]
   uint32_t thr;
-  uint32_t part;         // lookups per block work item
   uint32_t* long_ids;
-  Item* items;
-  uint32_t cap_long, cap_items, cap_slots;
+  LongRun* longs;
+  uint32_t cap_long;
 };
 
 struct ReduceArgs {
@@ -140,9 +140,10 @@ struct ReduceArgs {
   const uint32_t* vals;     // sorted values (uint32 or uint64, per value kind)
   const uint32_t* run_key;
   const uint32_t* run_start;
-  const Item* items;
-  float4* partials;         // [slots * C][KV*32]
-  uint32_t* done;           // [slots * C]
+  const LongRun* longs;
+  float4* partials;         // [2 * slices][KV*32]: head and tail piece of every slice
+  uint32_t* done;           // [2 * slices]: arrived pieces of a group, at its first piece's slot
+  uint32_t* done_run;       // [2 * slices]: arrived groups of a run, at its first piece's slot
   const void* grad;
   void* weights;
   float* momentum;
@@ -153,7 +154,8 @@ struct ReduceArgs {
   uint32_t T, B;
   int64_t grad_stride;      // elements per gradient row (sum of D, or D unpooled)
   float lr, eps;
-  uint32_t thr, part, C;
+  uint32_t thr, C;
+  uint32_t min_slice;       // fewest long-run lookups per warp slice
   uint32_t team_log2;       // lanes per team of the short-run phase: 2^team_log2
 };
 
@@ -432,9 +434,7 @@ struct ReduceKey {
 const void* reduce_kernel_f32(const ReduceKey& k);
 const void* reduce_kernel_f16(const ReduceKey& k);
 const void* reduce_kernel_bf16(const ReduceKey& k);
-inline size_t reduce_smem_bytes(int kv, int T) {
-  return (size_t)kWarps * kv * 32 * sizeof(float4) + 2 * (size_t)(T + 1) * sizeof(uint32_t);
-}
+inline size_t reduce_smem_bytes(int T) { return 2 * (size_t)(T + 1) * sizeof(uint32_t); }
 
 // atomic.cu (the index / offsets check reuses launch_hist with passes = 0)
 cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s, bool pdl);

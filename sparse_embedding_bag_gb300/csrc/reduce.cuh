@@ -77,10 +77,14 @@ struct Unroll {
   static constexpr int value = KV >= 4 ? 2 : 4;
 };
 
+// Long-run lookups per warp up to which the reduce cuts one slice per warp and
+// assigns it statically; above it, slices are handed out dynamically.
+constexpr uint32_t kStaticSlice = 64;
+
 // Minimum resident blocks per SM, by vectors per lane (register budget).
 template <int KV>
 struct MinBlocks {
-  static constexpr int value = KV == 1 ? 5 : (KV == 2 ? 4 : (KV == 4 ? 2 : 1));
+  static constexpr int value = KV <= 2 ? 4 : (KV == 4 ? 2 : 1);
 };
 
 // Sum over sorted positions [jb, je) of one run into acc by a team of lanes.
@@ -229,13 +233,123 @@ __device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* 
   return rs->cvec != 0;
 }
 
+// Index of the last long run whose place in the concatenation of long runs is
+// <= x (runs are in key order, places strictly increasing, the first is 0).
+// Warp-wide 32-way search: one load per lane and round.
+__device__ __forceinline__ uint32_t find_long(const LongRun* longs, uint32_t n, uint32_t x) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t lo = 0, hi = n;  // the answer is in [lo, hi); longs[lo].lpos <= x
+  while (hi - lo > 1) {
+    const uint32_t step = (hi - lo + 31) >> 5;
+    const uint32_t i = lo + lane * step;
+    const bool le = i < hi && longs[i].lpos <= x;
+    const uint32_t m = __popc(__ballot_sync(0xffffffffu, le));  // >= 1: lane 0 reads lo
+    lo += (m - 1) * step;
+    hi = min(lo + step, hi);
+  }
+  return lo;
+}
+
+// Pieces of a run cut by slice ends: the run covers slices sa .. sb of a row
+// chunk whose slices start at index `base`; the piece in slice q has partial row
+// slot 2*(base+q)+1 if it starts the run (q == sa), else 2*(base+q). Pieces are
+// combined in groups of kGroup slices: the last piece of a group to finish sums
+// the group into the slot of its first piece, and the last group to finish sums
+// the groups; all sums run in slice order, so the result does not depend on
+// scheduling.
+constexpr uint32_t kGroup = 16;
+
+// Cut of the concatenated long runs of one row chunk (positions [0, Ltot)) into
+// slices: nA slices of SLA lookups over [0, LA), then slices of SLB over the rest.
+struct Slicing {
+  uint32_t SLA, SLB, LA, nA, S1;
+  __device__ __forceinline__ uint32_t of(uint32_t p) const { return p < LA ? p / SLA : nA + (p - LA) / SLB; }
+  __device__ __forceinline__ uint32_t start(uint32_t s) const { return s < nA ? s * SLA : LA + (s - nA) * SLB; }
+};
+
+__device__ __forceinline__ size_t piece_slot(uint32_t base, uint32_t sa, uint32_t q) {
+  return 2 * (size_t)(base + q) + (q == sa ? 1u : 0u);
+}
+
+// Sum of the partial rows of n pieces q_0 = q0, q_k = (q0 / step + k) * step, by
+// the lane groups of a warp (group g adds q_g, q_{g+Pg}, ... in order, then the
+// groups are folded). Every lane group ends with the total.
+template <int KV>
+__device__ __forceinline__ void sum_pieces(const ReduceArgs& a, const RowShape& rs, uint32_t g, uint32_t li,
+                                           uint32_t base, uint32_t sa, uint32_t q0, uint32_t n,
+                                           uint32_t step, float4 (&acc)[KV]) {
+  constexpr int kAhead = 4;  // pieces loaded before any is added
+  const uint32_t Pg = 32u >> rs.lg;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t k0 = g; k0 < n; k0 += kAhead * Pg) {
+    float4 x[kAhead][KV];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const uint32_t k = k0 + u * Pg;
+      const uint32_t q = k == 0 ? q0 : (q0 / step + k) * step;
+      const float4* pp = a.partials + piece_slot(base, sa, q) * (KV * 32);
+#pragma unroll
+      for (int kv = 0; kv < KV; ++kv) {
+        const uint32_t v = li + (kv << rs.lg);
+        x[u][kv] = (k < n && v < rs.cvec) ? __ldcg(pp + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u)
+#pragma unroll
+      for (int kv = 0; kv < KV; ++kv) acc[kv] = f4_add(x[u][kv], acc[kv]);
+  }
+  team_fold<KV>(acc, 1u << rs.lg, 32);
+}
+
+// Arrival of one piece (acc: its sum in every lane group). Returns true in the
+// warp that completes the run, with the run's total in acc; false otherwise.
+template <int KV>
+__device__ __forceinline__ bool piece_arrive(const ReduceArgs& a, const RowShape& rs, uint32_t g, uint32_t li,
+                                             uint32_t base, uint32_t sa, uint32_t sb, uint32_t s,
+                                             float4 (&acc)[KV]) {
+  const uint32_t lane = threadIdx.x & 31;
+  auto store = [&](size_t slot) {
+    if (g == 0) {
+      float4* part = a.partials + slot * (KV * 32);
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const uint32_t v = li + (k << rs.lg);
+        if (v < rs.cvec) part[v] = acc[k];
+      }
+    }
+    __threadfence();
+    __syncwarp();
+  };
+  auto arrive = [&](uint32_t* ctr, uint32_t expect) {  // true in the last of `expect` arrivals
+    uint32_t prev = 0;
+    if (lane == 0) prev = atomicAdd(ctr, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev != expect - 1) return false;
+    __threadfence();
+    if (lane == 0) *ctr = 0;  // ready for the next call
+    return true;
+  };
+  store(piece_slot(base, sa, s));
+  // this piece's group of slices: pieces fs .. ls
+  const uint32_t fs = max(sa, s / kGroup * kGroup), ls = min(sb, s / kGroup * kGroup + kGroup - 1);
+  const size_t gslot = piece_slot(base, sa, fs);
+  if (!arrive(a.done + gslot, ls - fs + 1)) return false;
+  sum_pieces<KV>(a, rs, g, li, base, sa, fs, ls - fs + 1, 1, acc);
+  const uint32_t ga = sa / kGroup, gb = sb / kGroup;
+  if (ga == gb) return true;
+  store(gslot);  // the group's sum replaces its first piece
+  if (!arrive(a.done_run + piece_slot(base, sa, sa), gb - ga + 1)) return false;
+  sum_pieces<KV>(a, rs, g, li, base, sa, sa, gb - ga + 1, kGroup, acc);
+  return true;
+}
+
 template <typename emb_t, typename grad_t, int OPT, int VK, int KV>
 __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(ReduceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  float4* s_red = reinterpret_cast<float4*>(smem);                          // [8][KV*32]
-  uint32_t* s_hsc = reinterpret_cast<uint32_t*>(s_red + kWarps * KV * 32);  // [T+1]
-  int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);              // [T+1]
-  __shared__ uint32_t s_item, s_last;
+  uint32_t* s_hsc = reinterpret_cast<uint32_t*>(smem);  // [T+1]
+  int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);  // [T+1]
   constexpr int UNR = Unroll<KV>::value;
 
   pdl_wait();
@@ -245,105 +359,99 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
     s_hsc[i] = a.hsc[i];
     s_Do[i] = a.D_offsets[i];
   }
+  __syncthreads();
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t C = a.C;
+  const uint32_t W = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
 
-  // ---- phase 1: block work items of long runs (dynamic), one warp = one team.
-  const uint64_t total_items = (uint64_t)(*(volatile uint32_t*)&a.ctl->num_items) * C;
-  for (;;) {
-    if (threadIdx.x == 0) s_item = atomicAdd(&a.ctl->item_ctr, 1u);
-    __syncthreads();
-    const uint32_t w_all = s_item;
-    if (w_all >= total_items) break;
-    const uint32_t w = C == 1 ? w_all : w_all / C;
-    const uint32_t c = w_all - w * C;
-    const Item it = a.items[w];
-    const uint32_t P = it.P, p = it.q, ps = it.ps, pe = it.pe;
-    RowShape rs;
-    const bool active = make_shape<KV>(a, s_hsc, s_Do, it.key, c, &rs);
-    if (active) {
-      const uint32_t per = (pe - ps + kWarps - 1) / kWarps;
-      const uint32_t wb = min(ps + warp * per, pe), we = min(wb + per, pe);
-      const uint32_t Pg = 32u >> rs.lg;
-      const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
-      const uint32_t steps = (we - wb + Pg * UNR - 1) / (Pg * UNR);
-      float4 acc[KV];
-      team_gather<VK, grad_t, KV>(a, rs, wb, we, steps, Pg, g, li, acc);
-      team_fold<KV>(acc, 1u << rs.lg, 32);
-      if (g == 0) {
-#pragma unroll
-        for (int k = 0; k < KV; ++k) {
-          const uint32_t q = li + (k << rs.lg);
-          if (q < rs.cvec) s_red[warp * KV * 32 + q] = acc[k];
-        }
-      }
+  // ---- phase 1: the long runs, concatenated and cut into S1 slices per row
+  // chunk; one warp reduces one slice at a time. A run inside one
+  // slice is updated at once; a run cut by slice ends leaves one fp32 partial per
+  // piece, combined by the pieces that finish last (atomic counts, no waiting;
+  // see piece_arrive) in slice order before the row is updated. Little long-run
+  // work: one slice per warp, assigned statically. Much: about 16 slices per warp,
+  // handed out through one counter per warp index of a block (slice g belongs to
+  // counter g % kWarps), the next one requested while the current one is reduced.
+  const uint32_t NL = *(volatile uint32_t*)&a.ctl->num_long;
+  const uint32_t Ltot = *(volatile uint32_t*)&a.ctl->long_lookups;
+  if (Ltot > 0) {
+    const uint64_t per_warp = ((uint64_t)Ltot * C + W - 1) / W;
+    const bool dynamic = per_warp > kStaticSlice;
+    Slicing sl;
+    if (!dynamic) {
+      sl.SLA = sl.SLB = max((uint32_t)per_warp, a.min_slice);
+      sl.nA = (Ltot + sl.SLA - 1) / sl.SLA;
+      sl.LA = Ltot;
+    } else {
+      // about 16 slices per warp; with large slices, the last quarter of the
+      // lookups in slices 4x smaller, so that the warps that take the last
+      // slices finish together
+      sl.SLA = 1u << (32 - __clz((uint32_t)((per_warp + 15) / 16) - 1));  // pow2ceil(per_warp / 16)
+      sl.SLB = sl.SLA >= 256 ? sl.SLA / 4 : sl.SLA;
+      sl.nA = (uint32_t)((uint64_t)Ltot * 3 / 4 / sl.SLA);
+      sl.LA = sl.nA * sl.SLA;
     }
-    __syncthreads();
-    bool finish = active && P == 1;
-    if (active) {
-      const uint32_t u = threadIdx.x;
-      float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (u < rs.cvec) {
-#pragma unroll
-        for (int wi = 0; wi < kWarps; ++wi) G = f4_add(s_red[wi * KV * 32 + u], G);
+    sl.S1 = sl.nA + (Ltot - sl.LA + sl.SLB - 1) / sl.SLB;  // slices per row chunk
+    const uint32_t S1 = sl.S1;
+    const uint32_t NS = S1 * C;
+    uint32_t j = blockIdx.x;  // this warp's slice is j * kWarps + warp
+    for (;;) {
+      const uint32_t gs = j * kWarps + warp;
+      if (gs >= NS) break;
+      uint32_t nj = j + gridDim.x;
+      if (dynamic) {
+        if (lane == 0) nj = gridDim.x + atomicAdd(&a.ctl->slice_ctr[warp][0], 1u);
+        nj = __shfl_sync(0xffffffffu, nj, 0);
       }
-      if (P == 1) {
-        if (u < rs.cvec) s_red[u] = G;
-      } else {
-        const uint32_t slot0 = it.slot0;
-        float4* part = a.partials + ((size_t)(slot0 + p) * C + c) * (KV * 32);
-        if (u < rs.cvec) part[u] = G;
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          const uint32_t prev = atomicAdd(&a.done[(size_t)slot0 * C + c], 1u);
-          s_last = prev == P - 1;
+      const uint32_t c = gs / S1, s = gs - c * S1;
+      const uint32_t a0 = sl.start(s), b0 = min(sl.start(s + 1), Ltot);
+      for (uint32_t kl = find_long(a.longs, NL, a0); kl < NL; ++kl) {
+        const LongRun lr = a.longs[kl];
+        if (lr.lpos >= b0) break;
+        RowShape rs;
+        if (!make_shape<KV>(a, s_hsc, s_Do, lr.key, c, &rs)) continue;  // chunk past this row's end
+        const uint32_t p0 = lr.lpos, p1 = lr.lpos + lr.len;
+        const bool whole = p0 >= a0 && p1 <= b0;
+        const uint32_t Pg = 32u >> rs.lg;
+        const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
+        float4 wv[KV];
+        float m_old = 0.f;
+        const uint32_t jb = lr.start + (max(a0, p0) - p0), je = lr.start + (min(b0, p1) - p0);
+        const uint32_t steps = (je - jb + Pg * UNR - 1) / (Pg * UNR);
+        float4 acc[KV];
+        team_gather<VK, grad_t, KV>(a, rs, jb, je, steps, Pg, g, li, acc);
+        team_fold<KV>(acc, 1u << rs.lg, 32);
+        if (whole) {  // long runs: the row is read after the gather (registers)
+          load_row<emb_t, KV>(a, rs, true, g, li, wv);
+          if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+          update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
+          continue;
         }
-        __syncthreads();
-        if (s_last) {
-          __threadfence();
-          if (u < rs.cvec) {
-            float4 T4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (uint32_t q = 0; q < P; ++q)
-              T4 = f4_add(__ldcg(a.partials + ((size_t)(slot0 + q) * C + c) * (KV * 32) + u), T4);
-            s_red[u] = T4;
-          }
-          if (threadIdx.x == 0) a.done[(size_t)slot0 * C + c] = 0;  // ready for the next call
-          finish = true;
-        }
+        // a piece of a run cut by slice ends
+        if (!piece_arrive<KV>(a, rs, g, li, c * S1, sl.of(p0), sl.of(p1 - 1), s, acc)) continue;
+        load_row<emb_t, KV>(a, rs, true, g, li, wv);
+        if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
+        update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
       }
+      j = nj;
     }
-    __syncthreads();
-    if (finish && warp == 0) {
-      const uint32_t g = lane >> rs.lg, li = lane & ((1u << rs.lg) - 1);
-      float4 acc[KV], wv[KV];
-#pragma unroll
-      for (int k = 0; k < KV; ++k) {
-        const uint32_t q = li + (k << rs.lg);
-        acc[k] = q < rs.cvec ? s_red[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      load_row<emb_t, KV>(a, rs, true, g, li, wv);
-      float m_old = 0.f;
-      if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
-      update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
-    }
-    __syncthreads();
   }
 
-  // ---- phase 2: short runs; a warp holds 32/Lt teams of Lt lanes, one run (x chunk) each.
+  // ---- phase 2: short runs; a warp holds 32/Lt teams of Lt lanes, one run (x
+  // chunk) each per round; round q goes to warp q % W. All warps thus sweep the
+  // keys together, so rows updated at the same time lie close in memory.
   const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
-  const uint64_t tasks = (uint64_t)U * C;
+  const uint32_t tasks = U * C;  // < 2^31 (checked when the plan is made)
   const uint32_t Lt = 1u << a.team_log2, NT = 32u >> a.team_log2;
   const uint32_t team = lane >> a.team_log2, tl = lane & (Lt - 1);
-  const uint64_t stride = (uint64_t)gridDim.x * kWarps * NT;
-  for (uint64_t base = ((uint64_t)blockIdx.x * kWarps + warp) * NT; base < tasks; base += stride) {
-    const uint64_t task = base + team;
+  for (uint32_t base = gw * NT; base < tasks; base += W * NT) {
+    const uint32_t task = base + team;
     bool active = task < tasks;
     uint32_t start = 0, end = 0;
     RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
     if (active) {
-      const uint32_t r = C == 1 ? (uint32_t)task : (uint32_t)(task / C);
-      const uint32_t c = (uint32_t)(task - (uint64_t)r * C);
+      const uint32_t r = C == 1 ? task : task / C;
+      const uint32_t c = task - r * C;
       start = a.run_start[r];
       end = a.run_start[r + 1];
       active = end - start < a.thr && make_shape<KV>(a, s_hsc, s_Do, a.run_key[r], c, &rs);

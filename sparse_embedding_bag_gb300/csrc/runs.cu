@@ -7,15 +7,14 @@
 //     page's sorted_linear_indices_run / _cumulative_run_lengths / _num_runs);
 //   * the runs with at least max_segment_length_per_warp lookups (that page's
 //     *_find_long_segments), as an ordered compaction instead of an atomic
-//     append, together with their block work items: a long run is cut into
-//     parts of `part` lookups; runs with more than one part get one fp32
-//     partial-sum slot per part, combined later in part order.
+//     append, each with its place in the concatenation of all long runs (the
+//     prefix sum of their lengths), which the reduce cuts into equal slices.
 //
 // Each block owns a tile of kRleTile sorted keys and the runs whose first
 // lookup lies in it. A run that continues past the tile end has its end found
 // by a 32-lane parallel upper-bound search (a few rounds of one load per lane),
-// so every run's length is known inside the block that owns it. The four counts
-// (runs, long runs, work items, partial slots) of earlier tiles come from one
+// so every run's length is known inside the block that owns it. The three
+// counts (runs, long runs, lookups in long runs) of earlier tiles come from one
 // decoupled look-back per count, each walked 32 tiles at a time by a warp.
 #include "internal.cuh"
 
@@ -54,7 +53,7 @@ __device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ 
 __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   __shared__ uint32_t s_tile;
   __shared__ uint32_t s_scan[kWarps];
-  __shared__ uint32_t s_base[4];
+  __shared__ uint32_t s_base[3];
   __shared__ uint32_t s_last_key;
   __shared__ uint32_t s_head_pos[kRleTile + 1];
   pdl_wait();
@@ -106,8 +105,8 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   }
   __syncthreads();
 
-  // lengths, long runs, parts and partial slots of this thread's runs
-  uint32_t n_long = 0, n_items = 0, n_slots = 0;
+  // lengths, long runs and their lookups of this thread's runs
+  uint32_t n_long = 0, n_llook = 0;
   {
     uint32_t h = h0;
 #pragma unroll
@@ -115,28 +114,25 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
       if (heads & (1u << k)) {
         const uint32_t SL = s_head_pos[h + 1] - s_head_pos[h];
         if (SL >= a.thr) {
-          const uint32_t P = (SL + a.part - 1) / a.part;
           n_long += 1;
-          n_items += P;
-          if (P > 1) n_slots += P;
+          n_llook += SL;
         }
         ++h;
       }
     }
   }
-  uint32_t t_long, t_items, t_slots;
+  uint32_t t_long, t_llook;
   const uint32_t e_long = block_excl_scan(n_long, s_scan, &t_long);
-  const uint32_t e_items = block_excl_scan(n_items, s_scan, &t_items);
-  const uint32_t e_slots = block_excl_scan(n_slots, s_scan, &t_slots);
-  if (warp < 4) {  // one warp per count
-    const uint32_t agg = warp == 0 ? n_heads : warp == 1 ? t_long : warp == 2 ? t_items : t_slots;
-    const uint32_t b = lookback_warp(a.lb, tile, 4, warp, agg, a.ctl, a.sticky);
+  const uint32_t e_llook = block_excl_scan(n_llook, s_scan, &t_llook);
+  if (warp < 3) {  // one warp per count
+    const uint32_t agg = warp == 0 ? n_heads : warp == 1 ? t_long : t_llook;
+    const uint32_t b = lookback_warp(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);
     if (lane == 0) s_base[warp] = b;
   }
   __syncthreads();
 
   uint32_t r = s_base[0] + h0;
-  uint32_t kl = s_base[1] + e_long, ki = s_base[2] + e_items, ks = s_base[3] + e_slots;
+  uint32_t kl = s_base[1] + e_long, lp = s_base[2] + e_llook;
   bool overflow = false;
   uint32_t h = h0;
 #pragma unroll
@@ -151,19 +147,14 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
       }
       const uint32_t SL = end - start;
       if (SL >= a.thr) {
-        const uint32_t P = (SL + a.part - 1) / a.part;
-        if (kl < a.cap_long && ki + P <= a.cap_items && (P == 1 || ks + P <= a.cap_slots)) {
+        if (kl < a.cap_long) {
           a.long_ids[kl] = r;
-          for (uint32_t q = 0; q < P; ++q) {
-            const uint32_t ps = start + q * a.part;
-            a.items[ki + q] = Item{ps, min(ps + a.part, end), key[k], P > 1 ? ks : 0u, q, P, 0u, 0u};
-          }
+          a.longs[kl] = LongRun{start, SL, key[k], lp};
         } else {
           overflow = true;
         }
         kl += 1;
-        ki += P;
-        if (P > 1) ks += P;
+        lp += SL;
       }
       ++r;
       ++h;
@@ -177,8 +168,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
       a.run_start[U] = N;
     }
     a.ctl->num_long = s_base[1] + t_long;
-    a.ctl->num_items = s_base[2] + t_items;
-    a.ctl->num_slots = s_base[3] + t_slots;
+    a.ctl->long_lookups = s_base[2] + t_llook;
   }
 }
 
