@@ -444,17 +444,27 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
   const uint32_t tasks = U * C;  // < 2^31 (checked when the plan is made)
   const uint32_t Lt = 1u << a.team_log2, NT = 32u >> a.team_log2;
   const uint32_t team = lane >> a.team_log2, tl = lane & (Lt - 1);
+  // the bounds and key of the next round's run are loaded before this round's rows
+  auto meta = [&](uint32_t task, uint32_t& start, uint32_t& end, uint32_t& key) {
+    if (task < tasks) {
+      const uint32_t r = C == 1 ? task : task / C;
+      start = a.run_start[r];
+      end = a.run_start[r + 1];
+      key = a.run_key[r];
+    }
+  };
+  uint32_t n_start = 0, n_end = 0, n_key = 0;
+  meta(gw * NT + team, n_start, n_end, n_key);
   for (uint32_t base = gw * NT; base < tasks; base += W * NT) {
     const uint32_t task = base + team;
+    uint32_t start = n_start, end = n_end;
+    const uint32_t key = n_key;
+    meta(base + W * NT + team, n_start, n_end, n_key);
     bool active = task < tasks;
-    uint32_t start = 0, end = 0;
     RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
     if (active) {
       const uint32_t r = C == 1 ? task : task / C;
-      const uint32_t c = task - r * C;
-      start = a.run_start[r];
-      end = a.run_start[r + 1];
-      active = end - start < a.thr && make_shape<KV>(a, s_hsc, s_Do, a.run_key[r], c, &rs);
+      active = end - start < a.thr && make_shape<KV>(a, s_hsc, s_Do, key, task - r * C, &rs);
     }
     if (!__any_sync(0xffffffffu, active)) continue;
     if (!active) {
