@@ -38,6 +38,10 @@ DESCR = {
     "large": "large skewed: T=64 x 2M rows, D=128 fp16 weights, B=65536, L power law mean 30 max 500, "
              "Zipf(1.2) ids, sum, row-wise Adagrad",
 }
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# dominant kernel, from the ncu captures summarised under profiles/; a workload
+# without an entry for the current kernels reports null.
+TRAFFIC = {("dlrm", "reduce_update"): 21_146_880}  # profiles/k_reduce_dlrm.md
 
 
 def parse():
@@ -319,26 +323,29 @@ def main():
         stage_runs.append(E.emb_plan_stage_ms(plan))
     E.emb_plan_set_profiling(plan, False)
     stage = np.mean(np.array(stage_runs), axis=0)
-    names = ["linearise_hist", "radix_sort", "run_length", "long_partition", "reduce_update"]
-    if w.nobag and path == E.EMB_NOBAG_ATOMIC:
+    atomic = w.nobag and path == E.EMB_NOBAG_ATOMIC
+    names = ["linearise_hist", "radix_sort", "run_length", "-", "reduce_update"]
+    if atomic:
         names = ["index_check", "-", "-", "-", "atomic_scatter"]
-    dom = int(np.argmax(stage))
-    peak, peak_kind = peaks()
     total_bits = int(np.ceil(np.log2(max(int(w.hash_size_cumsum[-1]), 2))))
     passes = (total_bits + 7) // 8
+    # launches per stage: the dominant kernel is the one with the longest launch
+    launches = [1, 0 if atomic else passes, 0 if atomic else 1, 0, 1]
+    per_launch = [t / n if n else 0.0 for t, n in zip(stage, launches)]
+    dom = int(np.argmax(per_launch))
+    peak, peak_kind = peaks()
     vbytes = 8 if (w.per_sample_weights is not None or w.pooling == synth.MEAN) else 4
     N = n_local
     stage_bytes = {
         "linearise_hist": 8 * N + 8 * (w.T * w.B + 1),
         "radix_sort": N * (8 + 4 + vbytes) + (passes - 1) * N * 2 * (4 + vbytes),
         "run_length": 4 * N + 8 * uniq,
-        "long_partition": 8 * uniq,
         "reduce_update": reduce_bytes,
         "index_check": 8 * N,
         "atomic_scatter": reduce_bytes,
     }
     dom_name = names[dom]
-    achieved = stage_bytes.get(dom_name, 0) / (stage[dom] * 1e-3) / 1e9
+    achieved = stage_bytes.get(dom_name, 0) / launches[dom] / (per_launch[dom] * 1e-3) / 1e9
     red_achieved = reduce_bytes / (stage[4] * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers (H2D + call + status read)
@@ -368,7 +375,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_val = n_job / float(t[0])
 
-    kernels_per_step = 2 if (w.nobag and path == E.EMB_NOBAG_ATOMIC) else 4 + passes
+    kernels_per_step = 2 if atomic else 3 + passes  # hist, passes, run-length, reduce
     result = {
         "metric": METRIC,
         "value": n_job / (ms_job * 1e-3),
@@ -389,7 +396,7 @@ def main():
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None},
+                     "traffic": TRAFFIC.get((args.workload, dom_name))},
         "reduce_update": {"ms": float(stage[4]), "gbs": red_achieved, "frac": red_achieved / peak,
                           "bytes": reduce_bytes},
         "stage_ms": {n: float(v) for n, v in zip(names, stage) if n != "-"},

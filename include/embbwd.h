@@ -189,9 +189,9 @@ emb_status emb_plan_debug_runs(emb_plan* plan, int64_t capacity, int64_t* run_ke
 emb_status emb_plan_set_profiling(emb_plan* plan, int enable);
 
 /* Stage durations (ms) of the last profiled call; synchronises. Sorted path:
- * [0] linearise + histogram, [1] radix sort passes, [2] run-length encode,
- * [3] long-run partition, [4] reduce + optimizer. Atomic path: [0] index check,
- * [4] atomic scatter, others 0. Writes min(n, 5) values. */
+ * [0] linearise + histogram, [1] radix sort passes, [2] run-length encode and
+ * long-run partition (one kernel), [3] 0, [4] reduce + optimizer. Atomic path:
+ * [0] index check, [4] atomic scatter, others 0. Writes min(n, 5) values. */
 emb_status emb_plan_stage_ms(emb_plan* plan, float* ms, int32_t n);
 
 /* Static description of a status code. */

@@ -212,8 +212,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
   EMB_CUDA(launch_runs(ra, s, pdl));
-  EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel
-  EMB_TRY(record(p, 4, s));
+  EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel (no event 4)
 
   ReduceArgs r;
   r.ctl = p->ctl;
@@ -524,7 +523,7 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
     EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
     HistArgs ha{d, p->ctl, p->sticky, 0, (int)sort_tile_for(N), nullptr, nullptr};
     EMB_CUDA(launch_hist(ha, -1, p->T, s, pdl));
-    for (int i = 1; i <= 4; ++i) EMB_TRY(record(p, i, s));
+    EMB_TRY(record(p, 1, s));
     AtomicArgs aa{d, p->ctl, p->sticky, grad_output, static_cast<float*>(weights), p->d_wo,
                   (uint32_t)p->max_D, lr};
     EMB_CUDA(launch_nobag_atomic(aa, (int)p->gdt, p->T, s, pdl));
@@ -612,9 +611,15 @@ emb_status emb_plan_stage_ms(emb_plan* p, float* ms, int32_t n) {
   if (!p->events_ready || p->last_profiled == 0) return EMB_ERR_INVALID_ARG;
   DeviceGuard g(p->device);
   if (cudaEventSynchronize(p->ev[kStages]) != cudaSuccess) return EMB_ERR_CUDA;
+  // stage i runs from event from[i] to event to[i] (-1: stage not separate)
+  static const int kFromSorted[kStages] = {0, 1, 2, -1, 3}, kToSorted[kStages] = {1, 2, 3, -1, 5};
+  static const int kFromAtomic[kStages] = {0, -1, -1, -1, 1}, kToAtomic[kStages] = {1, -1, -1, -1, 5};
+  const int* from = p->last_profiled == 1 ? kFromSorted : kFromAtomic;
+  const int* to = p->last_profiled == 1 ? kToSorted : kToAtomic;
   for (int i = 0; i < kStages && i < n; ++i) {
     float v = 0.f;
-    if (cudaEventElapsedTime(&v, p->ev[i], p->ev[i + 1]) != cudaSuccess) return EMB_ERR_CUDA;
+    if (from[i] >= 0 && cudaEventElapsedTime(&v, p->ev[from[i]], p->ev[to[i]]) != cudaSuccess)
+      return EMB_ERR_CUDA;
     ms[i] = v;
   }
   return EMB_OK;

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
 constexpr int kBigItems = 16;
 
 template <int ITEMS, typename V>
-__global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 1) k_sort_pass(PassArgs a) {
+__global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_pass(PassArgs a) {
   constexpr int TILE = kThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* s_whist = reinterpret_cast<uint32_t*>(smem);  // [8][256]
