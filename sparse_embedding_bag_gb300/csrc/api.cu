@@ -57,7 +57,11 @@ struct emb_plan {
   struct RowSplit {
     int kv = 1;                     // 16-byte vectors per lane
     uint32_t C = 1;                 // chunks of kv*32 vectors per row
-    uint32_t team_log2 = 5;         // lanes per short-run team
+    // Segments of consecutive tables whose rows give the reduce the same team
+    // shape (chunks per row, lanes per lookup): first table of each, then T.
+    std::vector<uint32_t> segs;
+    uint32_t* d_segs = nullptr;
+    uint32_t* d_segkeys = nullptr;  // hash_size_cumsum of each segment's first table, then the total
   } split[2];
   int key_bits = 1;
   std::vector<uint32_t> hsc;
@@ -76,6 +80,7 @@ struct emb_plan {
   uint64_t* status = nullptr;
   uint32_t* run_key = nullptr;
   uint32_t* run_start = nullptr;
+  uint32_t* seg_runs = nullptr;  // [T+1]: first run of each segment of the call's split
   uint32_t* long_ids = nullptr;
   LongRun* longs = nullptr;
   float4* partials = nullptr;
@@ -97,12 +102,12 @@ struct emb_plan {
 namespace {
 
 const void* reduce_fn(const emb_plan* p, int opt, int vk) {
-  ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->split[opt].kv};
-  switch (p->wdt) {
-    case EMB_F32: return reduce_kernel_f32(k);
-    case EMB_F16: return reduce_kernel_f16(k);
-    default: return reduce_kernel_bf16(k);
-  }
+  const ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->split[opt].kv, p->split[opt].segs.size() > 2};
+  static const void* (*const entry[3][3])(const ReduceKey&) = {
+      {reduce_kernel_f32_f32, reduce_kernel_f32_f16, reduce_kernel_f32_bf16},
+      {reduce_kernel_f16_f32, reduce_kernel_f16_f16, reduce_kernel_f16_bf16},
+      {reduce_kernel_bf16_f32, reduce_kernel_bf16_f16, reduce_kernel_bf16_bf16}};
+  return entry[static_cast<int>(p->wdt)][static_cast<int>(p->gdt)](k);
 }
 
 emb_status record(emb_plan* p, int i, cudaStream_t s) {
@@ -211,6 +216,9 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.long_ids = p->long_ids;
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
+  ra.seg_keys = p->split[opt].d_segkeys;
+  ra.S = (uint32_t)p->split[opt].segs.size() - 1;
+  ra.seg_runs = p->seg_runs;
   EMB_CUDA(launch_runs(ra, s, pdl));
   EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel (no event 4)
 
@@ -219,6 +227,9 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.vals = static_cast<const uint32_t*>(p->vals[fin]);
   r.run_key = p->run_key;
   r.run_start = p->run_start;
+  r.seg_runs = p->seg_runs;
+  r.segs = p->split[opt].d_segs;
+  r.S = (uint32_t)p->split[opt].segs.size() - 1;
   r.longs = p->longs;
   r.partials = p->partials;
   r.done = p->done;
@@ -238,7 +249,6 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.thr = p->thr;
   r.min_slice = kMinSlice;
   r.C = p->split[opt].C;
-  r.team_log2 = p->split[opt].team_log2;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
@@ -322,11 +332,18 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 16 ? 2 : nvec <= 32 ? 4 : 2;
     else sp.kv = opt == 0 ? 2 : nvec <= 128 ? 4 : 8;
     sp.C = (uint32_t)((nvec + sp.kv * 32 - 1) / (sp.kv * 32));
-    // Short runs: teams of lanes as wide as the widest row's lane group (each lane
-    // holds kv vectors of a row; at most a warp).
-    const int per_lane = (std::min(nvec, sp.kv * 32) + sp.kv - 1) / sp.kv;
-    sp.team_log2 = 0;
-    while ((1 << sp.team_log2) < per_lane) ++sp.team_log2;
+    auto shape = [&](int32_t t) {  // (chunks per row, lanes per lookup) of table t
+      const int nv = (D_offsets[t + 1] - D_offsets[t]) / 4;
+      const int chunks = (nv + sp.kv * 32 - 1) / (sp.kv * 32);
+      const int per_lane = (std::min(nv, sp.kv * 32) + sp.kv - 1) / sp.kv;
+      int lanes = 1;
+      while (lanes < per_lane) lanes *= 2;
+      return std::make_pair(chunks, lanes);
+    };
+    sp.segs.clear();
+    for (int32_t t = 0; t < T; ++t)
+      if (t == 0 || shape(t) != shape(t - 1)) sp.segs.push_back((uint32_t)t);
+    sp.segs.push_back((uint32_t)T);
   }
   // the reduce counts (run x row chunk) tasks in 32 bits, with headroom
   if ((uint64_t)std::max<int64_t>(max_N, 1) * std::max(p->split[0].C, p->split[1].C) >= (1ull << 31)) {
@@ -412,6 +429,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
 
       {reinterpret_cast<void**>(&p->run_key), N * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->run_start), (N + 1) * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->seg_runs), (T + 1) * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[0].d_segkeys), p->split[0].segs.size() * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[1].d_segkeys), p->split[1].segs.size() * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[0].d_segs), p->split[0].segs.size() * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[1].d_segs), p->split[1].segs.size() * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->longs), p->cap_long * sizeof(LongRun)},
       {reinterpret_cast<void**>(&p->partials), 2 * (size_t)p->cap_slices * part_row},
@@ -440,6 +462,14 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   if (e == cudaSuccess) e = cudaMemcpy(p->d_Do, D_offsets, (T + 1) * sizeof(int32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_wo, weights_offsets, T * sizeof(int64_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_mo, mo.data(), T * sizeof(int64_t), cudaMemcpyHostToDevice);
+  for (const emb_plan::RowSplit& sp : p->split) {
+    std::vector<uint32_t> keys;
+    for (uint32_t t : sp.segs) keys.push_back(p->hsc[t]);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(sp.d_segs, sp.segs.data(), sp.segs.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(sp.d_segkeys, keys.data(), keys.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = sort_configure(p->props);
   if (e != cudaSuccess) {
     cudaGetLastError();

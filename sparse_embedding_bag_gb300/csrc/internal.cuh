@@ -133,6 +133,11 @@ struct RunsArgs {
   uint32_t* long_ids;
   LongRun* longs;
   uint32_t cap_long;
+  // Segments of consecutive tables (see ReduceArgs::segs): with S > 1, the first
+  // run of each segment is recorded (seg_runs[S] = number of runs).
+  const uint32_t* seg_keys;  // [S+1]: first linear index of each segment, then the total rows
+  uint32_t S;
+  uint32_t* seg_runs;        // [S+1]
 };
 
 struct ReduceArgs {
@@ -140,6 +145,9 @@ struct ReduceArgs {
   const uint32_t* vals;     // sorted values (uint32 or uint64, per value kind)
   const uint32_t* run_key;
   const uint32_t* run_start;
+  const uint32_t* seg_runs;    // [S+1]: first run of each segment (S > 1 only)
+  const uint32_t* segs;        // [S+1]: first table of each segment of tables with one team shape; segs[S] = T
+  uint32_t S;
   const LongRun* longs;
   float4* partials;         // [2 * slices][KV*32]: head and tail piece of every slice
   uint32_t* done;           // [2 * slices]: arrived pieces of a group, at its first piece's slot
@@ -156,7 +164,6 @@ struct ReduceArgs {
   float lr, eps;
   uint32_t thr, C;
   uint32_t min_slice;       // fewest long-run lookups per warp slice
-  uint32_t team_log2;       // lanes per team of the short-run phase: 2^team_log2
 };
 
 struct AtomicArgs {
@@ -330,6 +337,17 @@ __device__ __forceinline__ uint32_t lookback_warp(const LookbackCfg& lb, uint32_
   return excl;
 }
 
+// Table of a linear index: the last t with hash_size_cumsum[t] <= key (binary
+// search over a shared-memory copy of the T+1 entries).
+__device__ __forceinline__ uint32_t table_of(const uint32_t* s_hsc, uint32_t T, uint32_t key) {
+  uint32_t lo = 0, hi = T - 1;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi + 1) >> 1;
+    if (s_hsc[mid] <= key) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // t = bt / B without an integer divide: a float estimate corrected by one step
 // each way (the estimate is off by at most one for bt < 2^31, T < 2^22).
 __device__ __forceinline__ uint32_t div_by_B(uint32_t bt, uint32_t B, float invB) {
@@ -423,18 +441,27 @@ cudaError_t sort_configure(const DevProps& p);
 // runs.cu
 cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl);
 
-// reduce_*.cu: one entry per weight type.
+// reduce_<weight>_<grad>.cu: one entry per (weight type, gradient type) pair.
 struct ReduceKey {
   int grad_dtype;   // 0 f32, 1 f16, 2 bf16
   int optimizer;    // 0 SGD, 1 row-wise Adagrad
   int value_kind;   // ValueKind
   int kv;           // 1, 2, 4, 8 vectors of 4 per lane
+  bool multi;       // tables of several team shapes
 };
 // Kernel entry of the requested variant, or nullptr if the combination does not exist.
-const void* reduce_kernel_f32(const ReduceKey& k);
-const void* reduce_kernel_f16(const ReduceKey& k);
-const void* reduce_kernel_bf16(const ReduceKey& k);
-inline size_t reduce_smem_bytes(int T) { return 2 * (size_t)(T + 1) * sizeof(uint32_t); }
+#define EMB_REDUCE_ENTRY(w, g) const void* reduce_kernel_##w##_##g(const ReduceKey& k);
+EMB_REDUCE_ENTRY(f32, f32)
+EMB_REDUCE_ENTRY(f32, f16)
+EMB_REDUCE_ENTRY(f32, bf16)
+EMB_REDUCE_ENTRY(f16, f32)
+EMB_REDUCE_ENTRY(f16, f16)
+EMB_REDUCE_ENTRY(f16, bf16)
+EMB_REDUCE_ENTRY(bf16, f32)
+EMB_REDUCE_ENTRY(bf16, f16)
+EMB_REDUCE_ENTRY(bf16, bf16)
+#undef EMB_REDUCE_ENTRY
+inline size_t reduce_smem_bytes(int T) { return 4 * (size_t)(T + 1) * sizeof(uint32_t); }  // hsc, D, segments
 
 // atomic.cu (the index / offsets check reuses launch_hist with passes = 0)
 cudaError_t launch_nobag_atomic(const AtomicArgs& a, int grad_dtype, int T, cudaStream_t s, bool pdl);

@@ -38,15 +38,6 @@ struct ValT<VK_BAG_SCALED> {
   using type = uint64_t;
 };
 
-__device__ __forceinline__ uint32_t table_of(const uint32_t* s_hsc, uint32_t T, uint32_t key) {
-  uint32_t lo = 0, hi = T - 1;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi + 1) >> 1;
-    if (s_hsc[mid] <= key) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ uint32_t log2_pow2ceil32(uint32_t n) {
   // smallest l with 2^l >= n, capped at 5 (a warp)
   if (n >= 32) return 5;
@@ -78,13 +69,17 @@ struct Unroll {
 };
 
 // Long-run lookups per warp up to which the reduce cuts one slice per warp and
-// assigns it statically; above it, slices are handed out dynamically.
-constexpr uint32_t kStaticSlice = 64;
+// assigns it statically; above it, slices of at least kMinDynSlice lookups
+// (about 16 per warp) are handed out dynamically.
+constexpr uint32_t kStaticSlice = 256;
+constexpr uint32_t kMinDynSlice = 64;
 
 // Minimum resident blocks per SM, by vectors per lane (register budget).
-template <int KV>
+// Measured on GB300: with several team shapes (more loop state), 2 vectors per
+// lane run best at 3 blocks (80 registers) rather than 4 with spills.
+template <int KV, bool MULTI>
 struct MinBlocks {
-  static constexpr int value = KV <= 2 ? 4 : (KV == 4 ? 2 : 1);
+  static constexpr int value = KV == 1 ? 4 : (KV == 2 ? (MULTI ? 3 : 4) : (KV == 4 ? 2 : 1));
 };
 
 // Sum over sorted positions [jb, je) of one run into acc by a team of lanes.
@@ -215,11 +210,12 @@ __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& 
   }
 }
 
+// Shape of chunk c of the row with linear index `key` in table t; false if the
+// chunk lies past the row's end.
 template <int KV>
-__device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* s_hsc,
-                                           const int32_t* s_Do, uint32_t key, uint32_t c,
-                                           RowShape* rs) {
-  rs->t = table_of(s_hsc, a.T, key);
+__device__ __forceinline__ bool shape_in(const uint32_t* s_hsc, const int32_t* s_Do, uint32_t t,
+                                         uint32_t key, uint32_t c, RowShape* rs) {
+  rs->t = t;
   rs->idx = (int64_t)(key - s_hsc[rs->t]);
   const int32_t d0 = s_Do[rs->t], d1 = s_Do[rs->t + 1];
   rs->D = (uint32_t)(d1 - d0);
@@ -231,6 +227,13 @@ __device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* 
   const uint32_t per_lane = (rs->cvec + KV - 1) / KV;
   rs->lg = log2_pow2ceil32(per_lane);
   return rs->cvec != 0;
+}
+
+template <int KV>
+__device__ __forceinline__ bool make_shape(const ReduceArgs& a, const uint32_t* s_hsc,
+                                           const int32_t* s_Do, uint32_t key, uint32_t c,
+                                           RowShape* rs) {
+  return shape_in<KV>(s_hsc, s_Do, table_of(s_hsc, a.T, key), key, c, rs);
 }
 
 // Index of the last long run whose place in the concatenation of long runs is
@@ -345,11 +348,15 @@ __device__ __forceinline__ bool piece_arrive(const ReduceArgs& a, const RowShape
   return true;
 }
 
-template <typename emb_t, typename grad_t, int OPT, int VK, int KV>
-__global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(ReduceArgs a) {
+// MULTI: the tables form several segments of different team shapes (see
+// phase 2); without it, one shape serves every table and phase 2 is one sweep.
+template <typename emb_t, typename grad_t, int OPT, int VK, int KV, bool MULTI>
+__global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduce(ReduceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* s_hsc = reinterpret_cast<uint32_t*>(smem);  // [T+1]
   int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);  // [T+1]
+  uint32_t* s_seg = reinterpret_cast<uint32_t*>(s_Do + a.T + 1);  // [S+1] first table of each segment
+  uint32_t* s_segrun = s_seg + a.S + 1;                             // [S+1] first run of each segment
   constexpr int UNR = Unroll<KV>::value;
 
   pdl_wait();
@@ -358,6 +365,12 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
   for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) {
     s_hsc[i] = a.hsc[i];
     s_Do[i] = a.D_offsets[i];
+  }
+  if constexpr (MULTI) {
+    for (uint32_t i = threadIdx.x; i <= a.S; i += kThreads) {
+      s_seg[i] = a.segs[i];
+      s_segrun[i] = a.seg_runs[i];
+    }
   }
   __syncthreads();
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
       // about 16 slices per warp; with large slices, the last quarter of the
       // lookups in slices 4x smaller, so that the warps that take the last
       // slices finish together
-      sl.SLA = 1u << (32 - __clz((uint32_t)((per_warp + 15) / 16) - 1));  // pow2ceil(per_warp / 16)
+      sl.SLA = max(kMinDynSlice, 1u << (32 - __clz((uint32_t)((per_warp + 15) / 16) - 1)));  // pow2ceil(per_warp / 16)
       sl.SLB = sl.SLA >= 256 ? sl.SLA / 4 : sl.SLA;
       sl.nA = (uint32_t)((uint64_t)Ltot * 3 / 4 / sl.SLA);
       sl.LA = sl.nA * sl.SLA;
@@ -437,36 +450,19 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
     }
   }
 
-  // ---- phase 2: short runs; a warp holds 32/Lt teams of Lt lanes, one run (x
-  // chunk) each per round; round q goes to warp q % W. All warps thus sweep the
-  // keys together, so rows updated at the same time lie close in memory.
+  // ---- phase 2: short runs, by segments of consecutive tables whose rows give
+  // the same team shape (runs are in table order). In a segment a warp holds 32/Lt
+  // teams of Lt lanes (Lt from the row width), one run (x chunk) each per round;
+  // the rounds of all segments, in order, go round-robin to the warps. All warps
+  // thus sweep the keys together (rows updated at the same time lie close in
+  // memory), and narrow tables pack several runs per warp.
   const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
-  const uint32_t tasks = U * C;  // < 2^31 (checked when the plan is made)
-  const uint32_t Lt = 1u << a.team_log2, NT = 32u >> a.team_log2;
-  const uint32_t team = lane >> a.team_log2, tl = lane & (Lt - 1);
-  // the bounds and key of the next round's run are loaded before this round's rows
-  auto meta = [&](uint32_t task, uint32_t& start, uint32_t& end, uint32_t& key) {
-    if (task < tasks) {
-      const uint32_t r = C == 1 ? task : task / C;
-      start = a.run_start[r];
-      end = a.run_start[r + 1];
-      key = a.run_key[r];
-    }
-  };
-  uint32_t n_start = 0, n_end = 0, n_key = 0;
-  meta(gw * NT + team, n_start, n_end, n_key);
-  for (uint32_t base = gw * NT; base < tasks; base += W * NT) {
-    const uint32_t task = base + team;
-    uint32_t start = n_start, end = n_end;
-    const uint32_t key = n_key;
-    meta(base + W * NT + team, n_start, n_end, n_key);
-    bool active = task < tasks;
+  // One round of a team: run bounds [start, end) and key, table t, chunk c.
+  auto round = [&](bool active, uint32_t start, uint32_t end, uint32_t key, uint32_t t, uint32_t c,
+                   uint32_t Lt, uint32_t tl) {
     RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
-    if (active) {
-      const uint32_t r = C == 1 ? task : task / C;
-      active = end - start < a.thr && make_shape<KV>(a, s_hsc, s_Do, key, task - r * C, &rs);
-    }
-    if (!__any_sync(0xffffffffu, active)) continue;
+    active = active && end - start < a.thr && shape_in<KV>(s_hsc, s_Do, t, key, c, &rs);
+    if (!__any_sync(0xffffffffu, active)) return;
     if (!active) {
       rs = RowShape{0u, 0, 4u, 0u, 0u, 0u, 0};
       start = end = 0;
@@ -485,41 +481,91 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV>::value) k_reduce(Reduc
     team_gather<VK, grad_t, KV>(a, rs, start, end, steps, Pt, g, li, acc);
     team_fold<KV>(acc, 1u << rs.lg, Lt);
     update_row<emb_t, OPT, KV>(a, rs, active, g, li, tl, Lt, acc, wv, m_old);
+  };
+  if constexpr (!MULTI) {  // one team shape for all tables: one sweep over all runs
+    const uint32_t nvec = (uint32_t)(s_Do[1] - s_Do[0]) >> 2;
+    const uint32_t lgt = log2_pow2ceil32((min(nvec, (uint32_t)KV * 32) + KV - 1) / KV);
+    const uint32_t Lt = 1u << lgt, NT = 32u >> lgt;
+    const uint32_t team = lane >> lgt, tl = lane & (Lt - 1);
+    const uint32_t tasks = U * C;  // < 2^31 (checked when the plan is made)
+    // the bounds and key of the next round's run are loaded before this round's rows
+    auto meta = [&](uint32_t task, uint32_t& start, uint32_t& end, uint32_t& key) {
+      if (task < tasks) {
+        const uint32_t r = C == 1 ? task : task / C;
+        start = a.run_start[r];
+        end = a.run_start[r + 1];
+        key = a.run_key[r];
+      }
+    };
+    uint32_t n_start = 0, n_end = 0, n_key = 0;
+    meta(gw * NT + team, n_start, n_end, n_key);
+    for (uint32_t base = gw * NT; base < tasks; base += W * NT) {
+      const uint32_t task = base + team;
+      const uint32_t start = n_start, end = n_end, key = n_key;
+      meta(base + W * NT + team, n_start, n_end, n_key);
+      const uint32_t r = C == 1 ? task : task / C;
+      round(task < tasks, start, end, key, a.T == 1 ? 0u : table_of(s_hsc, a.T, key), task - r * C, Lt, tl);
+    }
+  } else {
+  uint32_t P = 0;  // rounds of the segments before
+  for (uint32_t sg = 0; sg < a.S; ++sg) {
+    const uint32_t t0 = s_seg[sg], t1 = s_seg[sg + 1];
+    const uint32_t R0 = s_segrun[sg], nr = s_segrun[sg + 1] - R0;
+    if (nr == 0) continue;
+    const uint32_t nvec = (uint32_t)(s_Do[t0 + 1] - s_Do[t0]) >> 2;
+    const uint32_t Ct = (nvec + KV * 32 - 1) / (KV * 32);  // chunks of a row
+    const uint32_t lgt = log2_pow2ceil32((min(nvec, (uint32_t)KV * 32) + KV - 1) / KV);
+    const uint32_t Lt = 1u << lgt, NT = 32u >> lgt;
+    const uint32_t team = lane >> lgt, tl = lane & (Lt - 1);
+    const uint32_t tasks = nr * Ct;
+    const uint32_t rounds = (tasks + NT - 1) / NT;
+    uint32_t q = (gw + W - P % W) % W;  // this warp's first round of the segment
+    P += rounds;
+    for (; q < rounds; q += W) {
+      const uint32_t task = q * NT + team;
+      uint32_t start = 0, end = 0, key = 0, t = t0;
+      if (task < tasks) {
+        const uint32_t r = R0 + (Ct == 1 ? task : task / Ct);
+        start = a.run_start[r];
+        end = a.run_start[r + 1];
+        key = a.run_key[r];
+        if (t1 - t0 > 1) t = t0 + table_of(s_hsc + t0, t1 - t0, key);
+      }
+      round(task < tasks, start, end, key, t, Ct == 1 ? 0u : task % Ct, Lt, tl);
+    }
+  }
   }
 }
 
-template <typename emb_t, typename grad_t, int OPT, int VK>
+template <typename emb_t, typename grad_t, int OPT, int VK, bool MULTI>
 const void* pick_kv(int kv) {
   switch (kv) {
-    case 1: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 1>);
-    case 2: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 2>);
-    case 4: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 4>);
-    case 8: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 8>);
+    case 1: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 1, MULTI>);
+    case 2: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 2, MULTI>);
+    case 4: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 4, MULTI>);
+    case 8: return reinterpret_cast<const void*>(&k_reduce<emb_t, grad_t, OPT, VK, 8, MULTI>);
     default: return nullptr;
   }
 }
 
-template <typename emb_t, typename grad_t>
+template <typename emb_t, typename grad_t, bool MULTI>
 const void* pick_vk(int opt, int vk, int kv) {
   if (opt == 0) {
-    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 0, VK_BAG>(kv);
-    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 0, VK_BAG_SCALED>(kv);
-    if (vk == VK_NOBAG) return pick_kv<emb_t, grad_t, 0, VK_NOBAG>(kv);
+    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 0, VK_BAG, MULTI>(kv);
+    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 0, VK_BAG_SCALED, MULTI>(kv);
+    if (vk == VK_NOBAG) return pick_kv<emb_t, grad_t, 0, VK_NOBAG, MULTI>(kv);
   } else if (opt == 1) {
-    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 1, VK_BAG>(kv);
-    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 1, VK_BAG_SCALED>(kv);
+    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 1, VK_BAG, MULTI>(kv);
+    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 1, VK_BAG_SCALED, MULTI>(kv);
   }
   return nullptr;
 }
 
-template <typename emb_t>
+// Kernel entry of the requested variant for one (weight, gradient) type pair.
+template <typename emb_t, typename grad_t>
 const void* pick_reduce(const ReduceKey& k) {
-  switch (k.grad_dtype) {
-    case 0: return pick_vk<emb_t, float>(k.optimizer, k.value_kind, k.kv);
-    case 1: return pick_vk<emb_t, __half>(k.optimizer, k.value_kind, k.kv);
-    case 2: return pick_vk<emb_t, __nv_bfloat16>(k.optimizer, k.value_kind, k.kv);
-    default: return nullptr;
-  }
+  return k.multi ? pick_vk<emb_t, grad_t, true>(k.optimizer, k.value_kind, k.kv)
+                 : pick_vk<emb_t, grad_t, false>(k.optimizer, k.value_kind, k.kv);
 }
 
 }  // namespace embbwd

@@ -1,0 +1,9 @@
+// Instantiations of the fused reduce + optimizer kernel for __nv_bfloat16 weights and
+// __half gradients (one file per type pair so the variants compile in parallel).
+#include "reduce.cuh"
+
+namespace embbwd {
+
+const void* reduce_kernel_bf16_f16(const ReduceKey& k) { return pick_reduce<__nv_bfloat16, __half>(k); }
+
+}  // namespace embbwd

@@ -1,0 +1,9 @@
+// Instantiations of the fused reduce + optimizer kernel for float weights and
+// float gradients (one file per type pair so the variants compile in parallel).
+#include "reduce.cuh"
+
+namespace embbwd {
+
+const void* reduce_kernel_f32_f32(const ReduceKey& k) { return pick_reduce<float, float>(k); }
+
+}  // namespace embbwd

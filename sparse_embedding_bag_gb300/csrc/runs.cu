@@ -13,7 +13,10 @@
 // Each block owns a tile of kRleTile sorted keys and the runs whose first
 // lookup lies in it. A run that continues past the tile end has its end found
 // by a 32-lane parallel upper-bound search (a few rounds of one load per lane),
-// so every run's length is known inside the block that owns it. The three
+// so every run's length is known inside the block that owns it. When the tables
+// form several segments (groups of consecutive tables the reduce treats alike),
+// a run whose key is the first of its segment (or follows empty segments)
+// records, for each segment it opens, that segment's first run. The three
 // counts (runs, long runs, lookups in long runs) of earlier tiles come from one
 // decoupled look-back per count, each walked 32 tiles at a time by a warp.
 #include "internal.cuh"
@@ -50,12 +53,18 @@ __device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ 
   return (uint32_t)lo;
 }
 
+// MULTI: the tables form several segments whose first runs are recorded.
+template <bool MULTI>
 __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   __shared__ uint32_t s_tile;
   __shared__ uint32_t s_scan[kWarps];
   __shared__ uint32_t s_base[3];
   __shared__ uint32_t s_last_key;
+  __shared__ uint32_t s_end_key;  // key at position N-1 (last tile only)
   __shared__ uint32_t s_head_pos[kRleTile + 1];
+  extern __shared__ uint32_t s_bkey[];  // [S+1] first key of each segment
+  if constexpr (MULTI)
+    for (uint32_t i = threadIdx.x; i <= a.S; i += kThreads) s_bkey[i] = a.seg_keys[i];
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
@@ -82,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   for (int k = 0; k < kRleItems; ++k) {
     const uint32_t before = k == 0 ? prev : key[k - 1];
     if (p0 + k < N && (p0 + k == 0 || key[k] != before)) heads |= 1u << k;
+    if (p0 + k == N - 1) s_end_key = key[k];
   }
   uint32_t n_heads;
   const uint32_t h0 = block_excl_scan(__popc(heads), s_scan, &n_heads);
@@ -142,6 +152,14 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
       if (r < N) {
         a.run_key[r] = key[k];
         a.run_start[r] = start;
+        if constexpr (MULTI) {  // first run of this key's segment (and of empty segments before it)
+          const uint32_t sg = table_of(s_bkey, a.S, key[k]);
+          const uint32_t before = k == 0 ? prev : key[k - 1];
+          if (start == 0 || before < s_bkey[sg]) {
+            const uint32_t s0 = start == 0 ? 0u : table_of(s_bkey, a.S, before) + 1;
+            for (uint32_t q = s0; q <= sg; ++q) a.seg_runs[q] = r;
+          }
+        }
       } else {
         overflow = true;
       }
@@ -166,6 +184,9 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
     if (U <= N) {
       a.ctl->num_runs = U;
       a.run_start[U] = N;
+      // segments after the last key's segment are empty
+      if constexpr (MULTI)
+        for (uint32_t q = table_of(s_bkey, a.S, s_end_key) + 1; q <= a.S; ++q) a.seg_runs[q] = U;
     }
     a.ctl->num_long = s_base[1] + t_long;
     a.ctl->long_lookups = s_base[2] + t_llook;
@@ -178,7 +199,9 @@ cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.N + kRleTile - 1) / kRleTile);
   RunsArgs arg = a;
   void* args[] = {&arg};
-  return launch_kernel(reinterpret_cast<const void*>(&k_runs), dim3(grid), dim3(kThreads), 0, s,
+  const void* fn = a.S > 1 ? reinterpret_cast<const void*>(&k_runs<true>)
+                           : reinterpret_cast<const void*>(&k_runs<false>);
+  return launch_kernel(fn, dim3(grid), dim3(kThreads), a.S > 1 ? (a.S + 1) * sizeof(uint32_t) : 0, s,
                        args, pdl);
 }
 
