@@ -89,6 +89,9 @@ struct emb_plan {
 
   uint32_t seq = 0;
   int reduce_grid[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  // Blocks that fit on the GPU at once: sort pass [large tiles][wide payload], k_runs [split].
+  int pass_cap[2][2] = {{0, 0}, {0, 0}};
+  int runs_cap[2] = {0, 0};
   cudaStream_t last_stream = nullptr;
   int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
   int64_t last_N = 0;
@@ -199,6 +202,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_out = p->vals[out];
     pa.pass = pass;
     pa.shift = pass * kRadixBits;
+    pa.ordered = (N + tile - 1) / tile <= p->pass_cap[tile == kThreads * 4 ? 0 : 1][wide ? 1 : 0];
     EMB_CUDA(launch_sort_pass(pa, wide, tile, s, pdl));
   }
   const int fin = (passes - 1) & 1;
@@ -213,6 +217,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.run_key = p->run_key;
   ra.run_start = p->run_start;
   ra.thr = p->thr;
+  ra.ordered = (N + kRleTile - 1) / kRleTile <= p->runs_cap[opt];
   ra.long_ids = p->long_ids;
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
@@ -471,6 +476,13 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       e = cudaMemcpy(sp.d_segkeys, keys.data(), keys.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = sort_configure(p->props);
+  if (e == cudaSuccess) {
+    for (int big = 0; big < 2; ++big)
+      for (int wide = 0; wide < 2; ++wide)
+        p->pass_cap[big][wide] = sort_pass_capacity(wide != 0, big ? kThreads * 16 : kThreads * 4, p->props.sms);
+    for (int opt = 0; opt < 2; ++opt)
+      p->runs_cap[opt] = runs_capacity((int)p->split[opt].segs.size() - 1, p->props.sms);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     cudaFree(p->arena);

@@ -112,6 +112,7 @@ struct PassArgs {
   void* vals_out;
   int pass;
   int shift;
+  int ordered;  // 1: tile = blockIdx.x (the whole grid fits on the GPU at once)
 };
 
 // A long run: sorted lookups [start, start + len) of linear index `key`;
@@ -130,6 +131,7 @@ struct RunsArgs {
   uint32_t* run_key;
   uint32_t* run_start;   // [U+1]
   uint32_t thr;
+  int ordered;  // 1: tile = blockIdx.x (the whole grid fits on the GPU at once)
   uint32_t* long_ids;
   LongRun* longs;
   uint32_t cap_long;
@@ -436,6 +438,9 @@ size_t sort_tile_for(int64_t N);  // lookups per block for hist and the passes
 // first_kind: the ValueKind of the pairs to write, or -1 to only check indices and offsets.
 cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s, bool pdl);
 cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl);
+// Blocks of the pass kernel (and of k_runs) that fit on the GPU at once.
+int sort_pass_capacity(bool wide_vals, int tile, int sms);
+int runs_capacity(int S, int sms);
 cudaError_t sort_configure(const DevProps& p);
 
 // runs.cu

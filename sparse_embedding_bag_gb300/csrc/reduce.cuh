@@ -457,11 +457,17 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
   // thus sweep the keys together (rows updated at the same time lie close in
   // memory), and narrow tables pack several runs per warp.
   const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
-  // One round of a team: run bounds [start, end) and key, table t, chunk c.
+  // One round of a team: run bounds [start, end) and key, table t (kAnyTable:
+  // found from the key), chunk c.
+  constexpr uint32_t kAnyTable = 0xffffffffu;
   auto round = [&](bool active, uint32_t start, uint32_t end, uint32_t key, uint32_t t, uint32_t c,
                    uint32_t Lt, uint32_t tl) {
     RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
-    active = active && end - start < a.thr && shape_in<KV>(s_hsc, s_Do, t, key, c, &rs);
+    active = active && end - start < a.thr;
+    if (active) {
+      if (t == kAnyTable) t = a.T == 1 ? 0u : table_of(s_hsc, a.T, key);
+      active = shape_in<KV>(s_hsc, s_Do, t, key, c, &rs);
+    }
     if (!__any_sync(0xffffffffu, active)) return;
     if (!active) {
       rs = RowShape{0u, 0, 4u, 0u, 0u, 0u, 0};
@@ -504,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
       const uint32_t start = n_start, end = n_end, key = n_key;
       meta(base + W * NT + team, n_start, n_end, n_key);
       const uint32_t r = C == 1 ? task : task / C;
-      round(task < tasks, start, end, key, a.T == 1 ? 0u : table_of(s_hsc, a.T, key), task - r * C, Lt, tl);
+      round(task < tasks, start, end, key, kAnyTable, task - r * C, Lt, tl);
     }
   } else {
   uint32_t P = 0;  // rounds of the segments before

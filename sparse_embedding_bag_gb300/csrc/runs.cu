@@ -67,9 +67,10 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
     for (uint32_t i = threadIdx.x; i <= a.S; i += kThreads) s_bkey[i] = a.seg_keys[i];
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
+  // tiles in look-back order (see k_sort_pass)
+  if (!a.ordered && threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
   __syncthreads();
-  const uint32_t tile = s_tile;
+  const uint32_t tile = a.ordered ? blockIdx.x : s_tile;
   const uint32_t N = (uint32_t)a.N;
   const uint32_t i0 = tile * kRleTile;
   const uint32_t p0 = i0 + threadIdx.x * kRleItems;
@@ -194,6 +195,17 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
 }
 
 }  // namespace
+
+int runs_capacity(int S, int sms) {
+  int blocks = 0;
+  const void* fn = S > 1 ? reinterpret_cast<const void*>(&k_runs<true>) : reinterpret_cast<const void*>(&k_runs<false>);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, S > 1 ? (S + 1) * sizeof(uint32_t) : 0) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return blocks * sms;
+}
 
 cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.N + kRleTile - 1) / kRleTile);

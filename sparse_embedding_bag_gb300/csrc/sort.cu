@@ -123,10 +123,13 @@ __global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_p
   pdl_wait();
   pdl_trigger();
 
-  if (threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
+  // Tiles in look-back order: the block index when every block of the grid can be
+  // resident at once (no block waits on one that cannot start), else a counter.
+  if (!a.ordered && threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
+  const uint32_t ghist = a.ctl->hist[a.pass][threadIdx.x];  // global count of digit threadIdx.x
   for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
   __syncthreads();
-  const uint32_t tile = s_misc[0];
+  const uint32_t tile = a.ordered ? blockIdx.x : s_misc[0];
   const int64_t i0 = (int64_t)tile * TILE;
   const int64_t i1 = min(i0 + TILE, N);
 
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_p
   }
   uint32_t tot;
   const uint32_t dstart = block_excl_scan(count, s_misc + 8, &tot);
-  const uint32_t gdig = block_excl_scan(a.ctl->hist[a.pass][dg], s_misc + 8, &tot);
+  const uint32_t gdig = block_excl_scan(ghist, s_misc + 8, &tot);
   const uint32_t excl = lookback_channel(a.lb, tile, kRadix, dg, count, a.ctl, a.sticky);
   s_dstart[dg] = dstart;
   s_gbase[dg] = gdig + excl - dstart;
@@ -268,22 +271,39 @@ cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s
                        args, pdl);
 }
 
+namespace {
+
+const void* pass_fn(bool wide_vals, int tile, size_t* sm) {
+  if (tile == kThreads * 4) {
+    *sm = wide_vals ? pass_smem<4, uint64_t>() : pass_smem<4, uint32_t>();
+    return wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<4, uint64_t>)
+                     : reinterpret_cast<const void*>(&k_sort_pass<4, uint32_t>);
+  }
+  *sm = wide_vals ? pass_smem<kBigItems, uint64_t>() : pass_smem<kBigItems, uint32_t>();
+  return wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<kBigItems, uint64_t>)
+                   : reinterpret_cast<const void*>(&k_sort_pass<kBigItems, uint32_t>);
+}
+
+}  // namespace
+
 cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)((a.N + tile - 1) / tile);
   PassArgs arg = a;
   void* args[] = {&arg};
-  const void* fn;
   size_t sm;
-  if (tile == kThreads * 4) {
-    fn = wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<4, uint64_t>)
-                   : reinterpret_cast<const void*>(&k_sort_pass<4, uint32_t>);
-    sm = wide_vals ? pass_smem<4, uint64_t>() : pass_smem<4, uint32_t>();
-  } else {
-    fn = wide_vals ? reinterpret_cast<const void*>(&k_sort_pass<kBigItems, uint64_t>)
-                   : reinterpret_cast<const void*>(&k_sort_pass<kBigItems, uint32_t>);
-    sm = wide_vals ? pass_smem<kBigItems, uint64_t>() : pass_smem<kBigItems, uint32_t>();
-  }
+  const void* fn = pass_fn(wide_vals, tile, &sm);
   return launch_kernel(fn, dim3(grid), dim3(kThreads), sm, s, args, pdl);
+}
+
+int sort_pass_capacity(bool wide_vals, int tile, int sms) {
+  size_t sm;
+  const void* fn = pass_fn(wide_vals, tile, &sm);
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return blocks * sms;
 }
 
 }  // namespace embbwd
