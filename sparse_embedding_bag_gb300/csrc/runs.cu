@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   if (!a.ordered && threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->tile_ctr[TC_RLE], 1u);
   __syncthreads();
   const uint32_t tile = a.ordered ? blockIdx.x : s_tile;
+  if (tile >= gridDim.x) {  // only if the control block was not zero: never index past the grid
+    if (threadIdx.x == 0) raise_error(a.ctl, a.sticky, kErrTimeout);
+    return;
+  }
   const uint32_t N = (uint32_t)a.N;
   const uint32_t i0 = tile * kRleTile;
   const uint32_t p0 = i0 + threadIdx.x * kRleItems;

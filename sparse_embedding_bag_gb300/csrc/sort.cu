@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_p
   for (int i = threadIdx.x; i < kWarps * kRadix; i += kThreads) s_whist[i] = 0;
   __syncthreads();
   const uint32_t tile = a.ordered ? blockIdx.x : s_misc[0];
+  if (tile >= gridDim.x) {  // only if the control block was not zero: never index past the grid
+    if (threadIdx.x == 0) raise_error(a.ctl, a.sticky, kErrTimeout);
+    return;
+  }
   const int64_t i0 = (int64_t)tile * TILE;
   const int64_t i1 = min(i0 + TILE, N);
 
