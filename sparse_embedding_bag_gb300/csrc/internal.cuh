@@ -236,6 +236,45 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratc
   return wbase + x - v;
 }
 
+// Exclusive scans of two values per thread at once (same barriers as one scan).
+// `scratch` holds 2 * kWarps words. Every thread of the block must call it.
+__device__ __forceinline__ void block_excl_scan2(uint32_t v0, uint32_t v1, uint32_t* scratch,
+                                                 uint32_t* e0, uint32_t* e1, uint32_t* t0,
+                                                 uint32_t* t1) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x0 = v0, x1 = v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y0 = __shfl_up_sync(0xffffffffu, x0, o);
+    const uint32_t y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
+    }
+  }
+  __syncthreads();  // scratch may still be read by a previous scan
+  if (lane == 31) {
+    scratch[warp] = x0;
+    scratch[kWarps + warp] = x1;
+  }
+  __syncthreads();
+  uint32_t b0 = 0, b1 = 0, s0 = 0, s1 = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t a0 = scratch[w], a1 = scratch[kWarps + w];
+    if (w < warp) {
+      b0 += a0;
+      b1 += a1;
+    }
+    s0 += a0;
+    s1 += a1;
+  }
+  *e0 = b0 + x0 - v0;
+  *e1 = b1 + x1 - v1;
+  *t0 = s0;
+  *t1 = s1;
+}
+
 // Decoupled look-back for one channel: publishes this tile's aggregate, walks
 // back over predecessors until an inclusive prefix is found, publishes its own
 // inclusive prefix and returns the exclusive one. Every wait is bounded: after

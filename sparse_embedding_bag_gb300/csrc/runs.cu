@@ -57,7 +57,7 @@ __device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ 
 template <bool MULTI>
 __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   __shared__ uint32_t s_tile;
-  __shared__ uint32_t s_scan[kWarps];
+  __shared__ uint32_t s_scan[2 * kWarps];
   __shared__ uint32_t s_base[3];
   __shared__ uint32_t s_last_key;
   __shared__ uint32_t s_end_key;  // key at position N-1 (last tile only)
@@ -136,9 +136,8 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
       }
     }
   }
-  uint32_t t_long, t_llook;
-  const uint32_t e_long = block_excl_scan(n_long, s_scan, &t_long);
-  const uint32_t e_llook = block_excl_scan(n_llook, s_scan, &t_llook);
+  uint32_t e_long, e_llook, t_long, t_llook;
+  block_excl_scan2(n_long, n_llook, s_scan, &e_long, &e_llook, &t_long, &t_llook);
   if (warp < 3) {  // one warp per count
     const uint32_t agg = warp == 0 ? n_heads : warp == 1 ? t_long : t_llook;
     const uint32_t b = lookback_warp(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);

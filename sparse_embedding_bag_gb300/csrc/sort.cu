@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_p
   uint32_t* s_whist = reinterpret_cast<uint32_t*>(smem);  // [8][256]
   uint32_t* s_dstart = s_whist + kWarps * kRadix;         // [256]
   uint32_t* s_gbase = s_dstart + kRadix;                  // [256]
-  uint32_t* s_misc = s_gbase + kRadix;                    // [16]
-  uint32_t* s_keys = s_misc + 16;                         // [TILE]
+  uint32_t* s_misc = s_gbase + kRadix;                    // [32]
+  uint32_t* s_keys = s_misc + 32;                         // [TILE]
   V* s_vals = reinterpret_cast<V*>(s_keys + TILE);        // [TILE]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = a.N;
@@ -178,9 +178,8 @@ __global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_p
     s_whist[w * kRadix + dg] = count;
     count += c;
   }
-  uint32_t tot;
-  const uint32_t dstart = block_excl_scan(count, s_misc + 8, &tot);
-  const uint32_t gdig = block_excl_scan(ghist, s_misc + 8, &tot);
+  uint32_t dstart, gdig, tot0, tot1;
+  block_excl_scan2(count, ghist, s_misc + 16, &dstart, &gdig, &tot0, &tot1);
   const uint32_t excl = lookback_channel(a.lb, tile, kRadix, dg, count, a.ctl, a.sticky);
   s_dstart[dg] = dstart;
   s_gbase[dg] = gdig + excl - dstart;
@@ -217,7 +216,7 @@ size_t hist_smem(int T) {
 
 template <int ITEMS, typename V>
 size_t pass_smem() {
-  return (kWarps * kRadix + 2 * kRadix + 16) * sizeof(uint32_t) +
+  return (kWarps * kRadix + 2 * kRadix + 32) * sizeof(uint32_t) +
          (size_t)kThreads * ITEMS * (sizeof(uint32_t) + sizeof(V));
 }
 
