@@ -75,8 +75,10 @@ def _load():
             lib.oracle_apply_row.argtypes = [i32, i32, vp, i64, i32, vp, vp, f64, f64]
             lib.oracle_backward.argtypes = [i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, vp,
                                             i32, i32, i32, vp, i32, f64, f64]
+            lib.oracle_forward.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, i64, vp, i32,
+                                           i32, vp]
             for name in ("oracle_sorted_pairs", "oracle_runs", "oracle_row_grads",
-                         "oracle_apply_row", "oracle_backward"):
+                         "oracle_apply_row", "oracle_backward", "oracle_forward"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.oracle_double_to_half.argtypes = [f64]
             lib.oracle_double_to_half.restype = ctypes.c_uint16
@@ -198,6 +200,21 @@ def backward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indice
                                    _p(weights), _p(momentum), _p(idx), _p(off), idx.size, _p(psw),
                                    int(bool(mean)), int(bool(nobag)), gcode, _p(g), optimizer,
                                    float(lr), float(eps)))
+
+
+def forward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices, offsets, *,
+            per_sample_weights=None, mean=False, out_dtype=F32):
+    """Forward pooled lookup: output [B, D_offsets[T]] of out_dtype (F32 -> float32,
+    F16 -> float16, BF16 -> uint16 holding bfloat16 bits)."""
+    hsc, Do = _c(hash_size_cumsum, np.int64), _c(D_offsets, np.int32)
+    wo = _c(weights_offsets, np.int64)
+    idx, off = _c(indices, np.int64), _c(offsets, np.int64)
+    psw = _c(per_sample_weights, np.float32)
+    out = np.zeros((B, int(Do[T])), {F32: np.float32, F16: np.float16, BF16: np.uint16}[out_dtype])
+    _check(_load().oracle_forward(T, B, _p(hsc), _p(Do), _p(wo), dtype_code(weights), _p(weights),
+                                  _p(idx), _p(off), idx.size, _p(psw), int(bool(mean)), out_dtype,
+                                  _p(out)))
+    return out
 
 
 def double_to_half_bits(x: float) -> int:

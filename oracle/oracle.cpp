@@ -30,6 +30,8 @@
 //           square root), applied to the de-duplicated row gradient;
 //   6. round w to its storage type (round to nearest, ties to even) and m to fp32.
 //
+// The forward pooled lookup (oracle_forward) is the adjoint of steps 1-4.
+//
 // Every function here is pinned by tests/test_oracle_*.py against brute force
 // (a dense one-hot matrix product), closed forms and invariants.
 #include <algorithm>
@@ -349,6 +351,48 @@ int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_o
     const int st2 = oracle_apply_row(optimizer, weight_dtype, weights, weights_offsets[t] + idx * D,
                                      D, G.data() + r * static_cast<int64_t>(Dmax), m, lr, eps);
     if (st2 != OK) return st2;
+  }
+  return OK;
+}
+
+// Forward pooled lookup (EmbeddingBag forward), written from the definition:
+// the output row of bag (t, b) is the sum over its lookups i of s_i times row
+// indices[i] of table t, with the same per-lookup scale as the backward
+// (s_i = per_sample_weight_i if weighted, times 1/L if mean pooling), so that
+// the forward is the adjoint of the backward's scatter. "tt_embeddings_cuda.cu",
+// cache_forward_kernel and reduce_output_kernel: a bag's output row is the sum
+// of the rows it indexes. Accumulated in double, rounded once to out_dtype;
+// out is [B, D_offsets[T]] and is overwritten (an empty bag gives zeros).
+int oracle_forward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_offsets,
+                   const int64_t* weights_offsets, int32_t weight_dtype, const void* weights,
+                   const int64_t* indices, const int64_t* offsets, int64_t N,
+                   const float* per_sample_weights, int32_t mean_pooling, int32_t out_dtype,
+                   void* out) {
+  if (T <= 0 || B <= 0 || !valid_tables(T, hsc, D_offsets)) return ERR_INVALID_ARG;
+  const int64_t BT = static_cast<int64_t>(T) * B;
+  if (offsets[0] != 0 || offsets[BT] != N) return ERR_INVALID_ARG;
+  for (int64_t bt = 0; bt < BT; ++bt)
+    if (offsets[bt + 1] < offsets[bt]) return ERR_INVALID_ARG;
+  for (int64_t bt = 0; bt < BT; ++bt) {
+    const int32_t t = static_cast<int32_t>(bt / B);
+    for (int64_t i = offsets[bt]; i < offsets[bt + 1]; ++i)
+      if (indices[i] < 0 || indices[i] >= hsc[t + 1] - hsc[t]) return ERR_INDEX_OUT_OF_RANGE;
+  }
+  const int64_t row_stride = D_offsets[T];
+  std::vector<double> acc;
+  for (int64_t bt = 0; bt < BT; ++bt) {
+    const int32_t t = static_cast<int32_t>(bt / B);
+    const int64_t b = bt % B;
+    const int32_t D = D_offsets[t + 1] - D_offsets[t];
+    const int64_t L = offsets[bt + 1] - offsets[bt];
+    acc.assign(static_cast<size_t>(D), 0.0);
+    for (int64_t i = offsets[bt]; i < offsets[bt + 1]; ++i) {
+      double s = per_sample_weights ? static_cast<double>(per_sample_weights[i]) : 1.0;
+      if (mean_pooling) s *= 1.0 / static_cast<double>(L);
+      const int64_t row = weights_offsets[t] + indices[i] * D;
+      for (int32_t d = 0; d < D; ++d) acc[d] += s * load_elem(weights, weight_dtype, row + d);
+    }
+    for (int32_t d = 0; d < D; ++d) store_elem(out, out_dtype, b * row_stride + D_offsets[t] + d, acc[d]);
   }
   return OK;
 }
