@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true", help="plain launches instead of programmatic dependent launches")
     ap.add_argument("--path", default="auto", choices=["auto", "sorted", "atomic"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", default="bwd", choices=["bwd", "fwd"],
+                    help="bwd: backward + update (the headline); fwd: forward pooled lookup")
     return ap.parse_args()
 
 
@@ -215,10 +217,119 @@ def run_reference(args):
     }))
 
 
+def run_forward(args):
+    """Forward pooled lookup on one GPU: the same timing rules as the backward."""
+    import torch
+    import oracle
+    from sparse_embedding_bag_gb300 import build as b
+    from sparse_embedding_bag_gb300 import device as dev
+    from sparse_embedding_bag_gb300 import embbwd as E
+    from sparse_embedding_bag_gb300 import synth
+    torch.cuda.set_device(0)
+    b.build()
+    E.load()
+    w = make_workload(args.workload, 0, "cuda:0")
+    if w.nobag:
+        raise SystemExit("the forward pooled lookup needs a pooled workload")
+    indices_h, offsets_h, _, psw_h = host_arrays(w)
+    dw = dev.to_device(w, "cuda:0")
+    plan = dev.make_plan(w, flags=E.EMB_FLAG_NO_PDL if args.no_pdl else 0)
+    out = torch.empty((w.B, int(w.D_offsets[-1])), dtype=torch.float32, device="cuda:0")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda:0")
+
+    def call():
+        dev.forward(plan, dw, 0, out)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    if E.emb_plan_status(plan) != E.EMB_OK:
+        raise SystemExit("device status error")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(0) as clocks:
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 0.6:
+            for _ in range(50):
+                flush.zero_()
+                graph.replay()
+            torch.cuda.synchronize()
+        for k in range(K):
+            flush.zero_()
+            starts[k].record()
+            graph.replay()
+            ends[k].record()
+        torch.cuda.synchronize()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+    N = int(indices_h.size)
+    lengths = np.diff(offsets_h)
+    t_of_lookup = np.repeat(np.arange(w.T * w.B) // w.B, lengths)
+    wsize = 4 if w.weight_dtype == synth.F32 else 2
+    fbytes = (8 * N + int(np.sum(w.dims[t_of_lookup].astype(np.int64))) * wsize +
+              w.B * int(w.D_offsets[-1]) * 4 + (4 * N if psw_h is not None else 0))
+    peak, peak_kind = peaks()
+    achieved = fbytes / (ms * 1e-3) / 1e9
+    # end to end: inputs from pinned host memory, the call, the output back to the host
+    pin = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_idx, h_off, h_psw = pin(indices_h), pin(offsets_h), pin(psw_h)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (h_idx, h_off, h_psw) if x is not None)
+    e2e = []
+    for k in range(min(max(3, K // 2), 200) + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dw.indices.copy_(h_idx, non_blocking=True)
+        dw.offsets.copy_(h_off, non_blocking=True)
+        if h_psw is not None:
+            dw.per_sample_weights.copy_(h_psw, non_blocking=True)
+        call()
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e.append(time.perf_counter() - t0)
+    e2e_s = statistics.median(e2e[2:])
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_done, el, runs = 0, 0.0, 0
+        while el < min(args.cpu_seconds, 10.0):
+            t1 = time.perf_counter()
+            oracle.forward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets,
+                           np.asarray(w.weights), indices_h, offsets_h, per_sample_weights=psw_h,
+                           mean=(w.pooling == synth.MEAN))
+            el += time.perf_counter() - t1
+            n_done += N
+            runs += 1
+        cpu = {"value": n_done / el, "unit": "lookups/s", "cores": 1, "kind": "oracle",
+               "sample": f"{runs} full forward(s) of the same workload, {el:.1f} s, single-threaded"}
+    print(json.dumps({
+        "metric": "embedding bag forward: lookups/sec and achieved HBM GB/s vs GB300 peak",
+        "op": "fwd", "value": N / (ms * 1e-3), "unit": "lookups/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "N": N, "output": "fp32 [B, sum D]",
+                   "l2": "256 MB buffer written between timed steps", "cuda_graph": True},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "kernel": "k_bag_fwd", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": N / e2e_s, "unit": "lookups/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "gpu_launches": K,
+        "clocks": clocks.summary(),
+    }, default=float))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "fwd":
+        return run_forward(args)
     import torch
     import torch.distributed as dist
 

@@ -143,6 +143,26 @@ emb_status emb_nobag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indic
                              const void* grad_output, float lr, emb_nobag_path path,
                              void* stream);
 
+/* Forward pooled lookup (EmbeddingBag forward) over the plan's tables:
+ *   output[b, D_offsets[t] + d] = sum over lookups i of bag (t, b) of
+ *                                 s_i * weights[weights_offsets[t] + indices[i]*D_t + d],
+ *   s_i = per_sample_weights[i] (if not NULL) times 1/L (EMB_POOL_MEAN, L = bag length),
+ * the scale the backward applies to the same lookup (the forward is the adjoint
+ * of the backward's scatter). "tt_embeddings_cuda.cu", cache_forward_kernel and
+ * reduce_output_kernel: a bag's output row is the sum of the rows it indexes.
+ *   weights     the plan's weight_dtype, layout as for the backward (read only).
+ *   indices, offsets, N, B, per_sample_weights  as for emb_bag_bwd_sgd.
+ *   output      [B, D_offsets[T]] of output_dtype (fp32, fp16 or bf16), overwritten
+ *               entirely: an empty bag gives zeros; rounded once from fp32 sums.
+ * Asynchronous on `stream`; uses no plan scratch, so it may run while no
+ * backward call of the plan is in flight on another stream. An index outside its
+ * table or malformed offsets latch EMB_ERR_INDEX_OUT_OF_RANGE / EMB_ERR_INVALID_ARG
+ * (read with emb_plan_status); the offending lookup or bag is left out. */
+emb_status emb_bag_fwd(emb_plan* plan, const void* weights, const int64_t* indices,
+                       const int64_t* offsets, int64_t N, int32_t B,
+                       const float* per_sample_weights, emb_pooling mode, void* output,
+                       emb_dtype output_dtype, void* stream);
+
 /* Allocation-free unpooled atomic SGD (the same update as emb_nobag_bwd_sgd with
  * EMB_NOBAG_ATOMIC), for callers that cannot allocate device memory when they run
  * it: inside a CUDA graph capture, under a runtime that owns all device memory,

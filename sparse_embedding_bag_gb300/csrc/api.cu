@@ -92,6 +92,7 @@ struct emb_plan {
   // Blocks that fit on the GPU at once: sort pass [large tiles][wide payload], k_runs [split].
   int pass_cap[2][2] = {{0, 0}, {0, 0}};
   int runs_cap[2] = {0, 0};
+  int fwd_grid[3] = {0, 0, 0};  // forward kernel grid per output type (0: not set up yet)
   cudaStream_t last_stream = nullptr;
   int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
   int64_t last_N = 0;
@@ -541,6 +542,61 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* moment
   const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
   return run_sorted(p, 1, vk, weights, momentum, indices, offsets, N, B, per_sample_weights,
                     grad_output, mode == EMB_POOL_MEAN, lr, eps, static_cast<cudaStream_t>(stream));
+}
+
+emb_status emb_bag_fwd(emb_plan* p, const void* weights, const int64_t* indices,
+                       const int64_t* offsets, int64_t N, int32_t B,
+                       const float* per_sample_weights, emb_pooling mode, void* output,
+                       emb_dtype output_dtype, void* stream) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  if (N < 0 || N > p->max_N || B <= 0 || B > p->max_B) return EMB_ERR_INVALID_ARG;
+  if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
+  if (output_dtype != EMB_F32 && output_dtype != EMB_F16 && output_dtype != EMB_BF16)
+    return EMB_ERR_INVALID_ARG;
+  if (!weights || !offsets || !output || (N > 0 && !indices)) return EMB_ERR_INVALID_ARG;
+  if (!aligned(weights, 4 * dtype_size(p->wdt)) || !aligned(output, 4 * dtype_size(output_dtype)) ||
+      !aligned(offsets, 8) || (indices && !aligned(indices, 8)) ||
+      (per_sample_weights && !aligned(per_sample_weights, 4)))
+    return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  const emb_plan::RowSplit& sp = p->split[0];
+  const void* fn = fwd_kernel(static_cast<int>(p->wdt), static_cast<int>(output_dtype), sp.kv);
+  if (!fn) return EMB_ERR_UNSUPPORTED;
+  const uint32_t S = (uint32_t)sp.segs.size() - 1;
+  const size_t sm = fwd_smem_bytes(p->T, (int)S);
+  int& grid = p->fwd_grid[output_dtype];
+  if (grid == 0) {  // first forward call with this output type: persistent grid
+    int blocks = 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, sm) != cudaSuccess) {
+      cudaGetLastError();
+      return EMB_ERR_CUDA;
+    }
+    grid = std::max(blocks, 1) * p->props.sms;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FwdArgs a;
+  a.weights = weights;
+  a.indices = indices;
+  a.offsets = offsets;
+  a.psw = per_sample_weights;
+  a.out = output;
+  a.sticky = p->sticky;
+  a.hsc = p->d_hsc;
+  a.D_offsets = p->d_Do;
+  a.weights_offsets = p->d_wo;
+  a.segs = sp.d_segs;
+  a.S = S;
+  a.T = (uint32_t)p->T;
+  a.B = (uint32_t)B;
+  a.N = N;
+  a.out_stride = p->Do[p->T];
+  a.mean = mode == EMB_POOL_MEAN;
+  void* args[] = {&a};
+  EMB_CUDA(launch_kernel(fn, dim3(grid), dim3(kThreads), sm, s, args, !(p->flags & EMB_FLAG_NO_PDL)));
+  p->last_stream = s;  // emb_plan_status waits for it
+  return EMB_OK;
 }
 
 emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,

@@ -168,6 +168,23 @@ struct ReduceArgs {
   uint32_t min_slice;       // fewest long-run lookups per warp slice
 };
 
+struct FwdArgs {
+  const void* weights;
+  const int64_t* indices;
+  const int64_t* offsets;          // [B*T+1]
+  const float* psw;                // nullable
+  void* out;                       // [B, out_stride]
+  uint32_t* sticky;                // error bits
+  const uint32_t* hsc;             // [T+1]
+  const int32_t* D_offsets;        // [T+1]
+  const int64_t* weights_offsets;  // [T]
+  const uint32_t* segs;            // [S+1] segments of tables with one team shape
+  uint32_t S, T, B;
+  int64_t N;
+  int64_t out_stride;              // D_offsets[T]
+  int mean;
+};
+
 struct AtomicArgs {
   DecodeArgs d;
   Ctl* ctl;
@@ -403,8 +420,14 @@ __device__ __forceinline__ uint32_t div_by_B(uint32_t bt, uint32_t B, float invB
 template <typename T>
 struct Vec4;
 
+// Raw<T>: the loaded bits of 4 elements (16 bytes for fp32, 8 for 16-bit types),
+// kept as loaded while a gather has loads in flight and widened to fp32 on use.
 template <>
 struct Vec4<float> {
+  using Raw = float4;
+  __device__ __forceinline__ static Raw load_raw(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ static Raw zero_raw() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ static float4 widen(Raw r) { return r; }
   __device__ __forceinline__ static float4 load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
   __device__ __forceinline__ static float4 load_plain(const float* p) { return *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -412,6 +435,10 @@ struct Vec4<float> {
 
 template <>
 struct Vec4<__half> {
+  using Raw = uint2;
+  __device__ __forceinline__ static Raw load_raw(const __half* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ static Raw zero_raw() { return make_uint2(0u, 0u); }
+  __device__ __forceinline__ static float4 widen(Raw r) { return cvt(r); }
   __device__ __forceinline__ static float4 cvt(uint2 u) {
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
     const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
@@ -431,6 +458,10 @@ struct Vec4<__half> {
 
 template <>
 struct Vec4<__nv_bfloat16> {
+  using Raw = uint2;
+  __device__ __forceinline__ static Raw load_raw(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ __forceinline__ static Raw zero_raw() { return make_uint2(0u, 0u); }
+  __device__ __forceinline__ static float4 widen(Raw r) { return cvt(r); }
   __device__ __forceinline__ static float4 cvt(uint2 u) {
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
@@ -484,6 +515,10 @@ cudaError_t sort_configure(const DevProps& p);
 
 // runs.cu
 cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl);
+
+// forward.cu: forward pooled lookup kernel of (weight type, output type, kv), or nullptr.
+const void* fwd_kernel(int weight_dtype, int out_dtype, int kv);
+size_t fwd_smem_bytes(int T, int S);
 
 // reduce_<weight>_<grad>.cu: one entry per (weight type, gradient type) pair.
 struct ReduceKey {

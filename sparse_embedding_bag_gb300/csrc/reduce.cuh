@@ -63,7 +63,7 @@ struct RowShape {
 };
 
 // Lookups gathered per lane group and step, unrolled for memory-level parallelism.
-template <int KV>
+template <int KV, typename grad_t>
 struct Unroll {
   static constexpr int value = KV >= 4 ? 2 : 4;
 };
@@ -92,7 +92,7 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
                                             uint32_t je, uint32_t steps, uint32_t P, uint32_t g,
                                             uint32_t li, float4 (&acc)[KV]) {
   using V = typename ValT<VK>::type;
-  constexpr int UNR = Unroll<KV>::value;
+  constexpr int UNR = Unroll<KV, grad_t>::value;
   const V* vals = reinterpret_cast<const V*>(a.vals);
   // Byte address of gradient row 0 of this run's table chunk; a lookup adds
   // (bag or lookup id) * stride with one 32x32->64 multiply. For pooled rows the
@@ -122,7 +122,7 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
       ok[u] = j < je;
       v[u] = ok[u] ? vals[j] : (V)0;
     }
-    float4 x[UNR][KV];
+    typename Vec4<grad_t>::Raw x[UNR][KV];  // loaded bits, widened when added
     float scale[UNR];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -131,15 +131,16 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
       if constexpr (VK == VK_BAG_SCALED) scale[u] = __uint_as_float((uint32_t)(v[u] >> 32));
 #pragma unroll
       for (int k = 0; k < KV; ++k)
-        x[u][k] = (ok[u] && on[k]) ? Vec4<grad_t>::load(reinterpret_cast<const grad_t*>(row + col[k]))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u][k] = (ok[u] && on[k]) ? Vec4<grad_t>::load_raw(reinterpret_cast<const grad_t*>(row + col[k]))
+                                   : Vec4<grad_t>::zero_raw();
     }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
-        if constexpr (VK == VK_BAG_SCALED) acc[k] = f4_fma(scale[u], x[u][k], acc[k]);
-        else acc[k] = f4_add(x[u][k], acc[k]);
+        const float4 f = Vec4<grad_t>::widen(x[u][k]);
+        if constexpr (VK == VK_BAG_SCALED) acc[k] = f4_fma(scale[u], f, acc[k]);
+        else acc[k] = f4_add(f, acc[k]);
       }
     }
   }
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
   int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);  // [T+1]
   uint32_t* s_seg = reinterpret_cast<uint32_t*>(s_Do + a.T + 1);  // [S+1] first table of each segment
   uint32_t* s_segrun = s_seg + a.S + 1;                             // [S+1] first run of each segment
-  constexpr int UNR = Unroll<KV>::value;
+  constexpr int UNR = Unroll<KV, grad_t>::value;
 
   pdl_wait();
   pdl_trigger();

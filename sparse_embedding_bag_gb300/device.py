@@ -67,6 +67,19 @@ def step(plan, dw: DeviceWorkload, path: int = E.EMB_NOBAG_AUTO, stream=None, N=
                                          w.lr, w.eps, stream)
 
 
+def forward(plan, dw: DeviceWorkload, out_dtype: int = 0, out=None, stream=None):
+    """Forward pooled lookup through the C ABI into `out` (allocated if None):
+    a [B, sum D] tensor of out_dtype (0 fp32, 1 fp16, 2 bf16). Returns `out`."""
+    import torch
+    w = dw.w
+    if out is None:
+        tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[out_dtype]
+        out = torch.empty((w.B, int(w.D_offsets[-1])), dtype=tdt, device=dw.weights.device)
+    E.emb_bag_fwd(plan, dw.weights, dw.indices, dw.offsets, w.N, w.B, dw.per_sample_weights,
+                  w.pooling, out, out_dtype, stream)
+    return out
+
+
 def weights_numpy(dw: DeviceWorkload) -> np.ndarray:
     """Device weights back as numpy in the workload's storage representation."""
     a = dw.weights.cpu().numpy()

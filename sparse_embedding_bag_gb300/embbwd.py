@@ -28,7 +28,8 @@ EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 # Every symbol include/embbwd.h declares (checked by the tests against the header).
 EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_rowwise_adagrad",
            "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
-           "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc")
+           "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc",
+           "emb_bag_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,7 @@ def load(path: str = LIB_PATH):
             "emb_status_string": [c_int],
             "emb_nobag_bwd_sgd_atomic_noalloc": [c_int, i32, vp, vp, i32, vp, vp, vp, i64, i32, vp,
                                                  c_int, f32, vp, vp],
+            "emb_bag_fwd": [vp, vp, vp, vp, i64, i32, vp, c_int, vp, c_int, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -152,6 +154,14 @@ def emb_nobag_bwd_sgd(plan, weights, indices, offsets, N, B, grad_output, lr,
     st = load().emb_nobag_bwd_sgd(plan, _ptr(weights), _ptr(indices), _ptr(offsets), int(N),
                                   int(B), _ptr(grad_output), float(lr), int(path), _stream(stream))
     return _check(st, "emb_nobag_bwd_sgd")
+
+
+def emb_bag_fwd(plan, weights, indices, offsets, N, B, per_sample_weights, mode, output,
+                output_dtype, stream=None):
+    st = load().emb_bag_fwd(plan, _ptr(weights), _ptr(indices), _ptr(offsets), int(N), int(B),
+                            _ptr(per_sample_weights), int(mode), _ptr(output), int(output_dtype),
+                            _stream(stream))
+    return _check(st, "emb_bag_fwd")
 
 
 def emb_plan_status(plan):
