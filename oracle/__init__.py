@@ -40,7 +40,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, F16, BF16 = 0, 1, 2
-SGD, ROWWISE_ADAGRAD = 0, 1
+SGD, ROWWISE_ADAGRAD, ADAGRAD = 0, 1, 2
 SUM, MEAN = 0, 1
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "index out of range"}
@@ -77,8 +77,11 @@ def _load():
                                             i32, i32, i32, vp, i32, f64, f64]
             lib.oracle_forward.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, i64, vp, i32,
                                            i32, vp]
+            lib.oracle_dense_grad.argtypes = [i32, i32, vp, vp, vp, i64, i32, vp, vp, vp, i64, vp,
+                                              i32, i32, i32, vp]
             for name in ("oracle_sorted_pairs", "oracle_runs", "oracle_row_grads",
-                         "oracle_apply_row", "oracle_backward", "oracle_forward"):
+                         "oracle_apply_row", "oracle_backward", "oracle_forward",
+                         "oracle_dense_grad"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.oracle_double_to_half.argtypes = [f64]
             lib.oracle_double_to_half.restype = ctypes.c_uint16
@@ -171,8 +174,13 @@ def apply_row(optimizer, weights, row_offset, D, g, momentum=None, momentum_inde
     m = None
     if optimizer == ROWWISE_ADAGRAD:
         m = np.array([momentum[momentum_index]], np.float32)
+    elif optimizer == ADAGRAD:
+        m = np.array(momentum[momentum_index:momentum_index + D], np.float32)
     _check(_load().oracle_apply_row(optimizer, code, _p(weights), row_offset, D, _p(gd), _p(m),
                                     float(lr), float(eps)))
+    if optimizer == ADAGRAD:
+        momentum[momentum_index:momentum_index + D] = m
+        return m
     if m is not None:
         momentum[momentum_index] = m[0]
         return m[0]
@@ -200,6 +208,24 @@ def backward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indice
                                    _p(weights), _p(momentum), _p(idx), _p(off), idx.size, _p(psw),
                                    int(bool(mean)), int(bool(nobag)), gcode, _p(g), optimizer,
                                    float(lr), float(eps)))
+
+
+def dense_grad(T, B, hash_size_cumsum, D_offsets, weights_offsets, extent, indices, offsets,
+               grad_output, *, out_dtype=F32, per_sample_weights=None, mean=False, nobag=False,
+               grad_dtype=None):
+    """Dense-gradient mode: [extent] buffer (weights layout) of out_dtype, zero except the
+    de-duplicated row gradients of the touched rows."""
+    hsc, Do = _c(hash_size_cumsum, np.int64), _c(D_offsets, np.int32)
+    wo = _c(weights_offsets, np.int64)
+    idx, off = _c(indices, np.int64), _c(offsets, np.int64)
+    psw = _c(per_sample_weights, np.float32)
+    g = np.ascontiguousarray(grad_output)
+    gcode = dtype_code(g) if grad_dtype is None else grad_dtype
+    out = np.empty(int(extent), {F32: np.float32, F16: np.float16, BF16: np.uint16}[out_dtype])
+    _check(_load().oracle_dense_grad(T, B, _p(hsc), _p(Do), _p(wo), int(extent), out_dtype,
+                                     _p(out), _p(idx), _p(off), idx.size, _p(psw), int(bool(mean)),
+                                     int(bool(nobag)), gcode, _p(g)))
+    return out
 
 
 def forward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices, offsets, *,

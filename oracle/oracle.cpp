@@ -293,10 +293,23 @@ int oracle_row_grads(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_
 }
 
 // Step 5-6 on one row: applies the optimizer to row `w` (storage dtype) of
-// length D with gradient g (double) and, for row-wise Adagrad, the fp32 state m.
-//   optimizer 0 = SGD, 1 = row-wise Adagrad.
+// length D with gradient g (double) and its fp32 state m (one value for
+// row-wise Adagrad, D values for elementwise Adagrad).
+//   optimizer 0 = SGD, 1 = row-wise Adagrad, 2 = elementwise Adagrad
+//   ("tt_embeddings_cuda.cu", update_tt_cores_adagrad_kernel: per element
+//   m <- m + g^2, w <- w - lr * g / (sqrt(m) + eps)).
 int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int64_t row_offset,
                      int32_t D, const double* g, float* m, double lr, double eps) {
+  if (optimizer == 2) {
+    if (!m) return ERR_INVALID_ARG;
+    for (int32_t d = 0; d < D; ++d) {
+      const double m_new = static_cast<double>(m[d]) + g[d] * g[d];
+      const double w = load_elem(weights, weight_dtype, row_offset + d);
+      store_elem(weights, weight_dtype, row_offset + d, w - lr * g[d] / (std::sqrt(m_new) + eps));
+      m[d] = static_cast<float>(m_new);
+    }
+    return OK;
+  }
   if (optimizer == 0) {
     for (int32_t d = 0; d < D; ++d) {
       const double w = load_elem(weights, weight_dtype, row_offset + d);
@@ -319,8 +332,10 @@ int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int
 
 // The whole pooled (nobag == 0) or unpooled (nobag != 0) backward with the
 // optimizer applied in place to each unique touched row. Untouched rows are
-// not written. momentum_offsets may be NULL (then row idx of table t uses
-// momentum[hash_size_cumsum[t] + idx]); momentum is ignored for SGD.
+// not written. Row-wise Adagrad: momentum_offsets may be NULL (then row idx of
+// table t uses momentum[hash_size_cumsum[t] + idx]). Elementwise Adagrad: the
+// state has the layout of the weights (momentum[weights_offsets[t] + idx*D + d]).
+// momentum is ignored for SGD.
 int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_offsets,
                     const int64_t* weights_offsets, const int64_t* momentum_offsets,
                     int32_t weight_dtype, void* weights, float* momentum,
@@ -347,10 +362,45 @@ int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_o
     if (optimizer == 1) {
       const int64_t mo = momentum_offsets ? momentum_offsets[t] : hsc[t];
       m = momentum + mo + idx;
+    } else if (optimizer == 2) {
+      m = momentum + weights_offsets[t] + idx * D;
     }
     const int st2 = oracle_apply_row(optimizer, weight_dtype, weights, weights_offsets[t] + idx * D,
                                      D, G.data() + r * static_cast<int64_t>(Dmax), m, lr, eps);
     if (st2 != OK) return st2;
+  }
+  return OK;
+}
+
+// Dense-gradient mode: the de-duplicated row gradient of every touched row,
+// stored (rounded once to out_dtype) into `grad_weights`, which has the layout of
+// the weights and is zeroed first over [0, extent) ("embedding_backward_split_
+// template.cu", the dense variant: grad_dev_weights = zeros_like(dev_weights),
+// then grad_sum stored at weights_offset + idx * D per touched row).
+int oracle_dense_grad(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_offsets,
+                      const int64_t* weights_offsets, int64_t extent, int32_t out_dtype,
+                      void* grad_weights, const int64_t* indices, const int64_t* offsets,
+                      int64_t N, const float* per_sample_weights, int32_t mean_pooling,
+                      int32_t nobag, int32_t grad_dtype, const void* grad_output) {
+  if (T <= 0 || B <= 0) return ERR_INVALID_ARG;
+  for (int64_t e = 0; e < extent; ++e) store_elem(grad_weights, out_dtype, e, 0.0);
+  if (N == 0) return OK;
+  int32_t Dmax = 0;
+  for (int32_t t = 0; t < T; ++t) Dmax = std::max(Dmax, D_offsets[t + 1] - D_offsets[t]);
+  std::vector<int64_t> keys(static_cast<size_t>(N));
+  std::vector<double> G(static_cast<size_t>(N) * static_cast<size_t>(Dmax));
+  int64_t U = 0;
+  const int st = oracle_row_grads(T, B, hsc, D_offsets, indices, offsets, N, per_sample_weights,
+                                  mean_pooling, nobag, grad_dtype, grad_output, Dmax, keys.data(),
+                                  G.data(), &U);
+  if (st != OK) return st;
+  for (int64_t r = 0; r < U; ++r) {
+    const int32_t t = table_of_key(T, hsc, keys[r]);
+    const int64_t idx = keys[r] - hsc[t];
+    const int32_t D = D_offsets[t + 1] - D_offsets[t];
+    for (int32_t d = 0; d < D; ++d)
+      store_elem(grad_weights, out_dtype, weights_offsets[t] + idx * D + d,
+                 G[static_cast<size_t>(r) * Dmax + d]);
   }
   return OK;
 }
