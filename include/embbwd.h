@@ -128,6 +128,35 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* plan, void* weights, float* mom
                                        const void* grad_output, emb_pooling mode, float lr,
                                        float eps, void* stream);
 
+/* Pooled backward + elementwise Adagrad, in place on `weights` and fp32 `momentum`,
+ * whose layout is that of the weights (momentum[weights_offsets[t] + idx*D_t + d],
+ * 16-byte aligned): for every unique row, with G its de-duplicated gradient,
+ *   m_d <- m_d + G_d^2 ;  w_d <- w_d - lr * G_d / (sqrt(m_d) + eps)
+ * ("tt_embeddings_cuda.cu", update_tt_cores_adagrad_kernel). Other arguments as
+ * for emb_bag_bwd_sgd; rows of any supported width. */
+emb_status emb_bag_bwd_adagrad(emb_plan* plan, void* weights, float* momentum,
+                               const int64_t* indices, const int64_t* offsets, int64_t N,
+                               int32_t B, const float* per_sample_weights,
+                               const void* grad_output, emb_pooling mode, float lr, float eps,
+                               void* stream);
+
+/* Dense-gradient mode: instead of updating, writes the de-duplicated gradient G of
+ * every touched row into `grad_weights`, a buffer of the plan's weight_dtype with
+ * the layout of the weights (row idx of table t at grad_weights[weights_offsets[t] +
+ * idx*D_t]), after zeroing it over the plan's whole weights extent (the largest
+ * weights_offsets[t] + rows_t*D_t), so untouched rows read zero ("embedding_backward_
+ * split_template.cu", the dense variant: grad_dev_weights = zeros_like(dev_weights),
+ * then grad_sum stored per touched row). G is rounded once to the storage type.
+ * Pooled: arguments as for emb_bag_bwd_sgd without lr. Unpooled: as for
+ * emb_nobag_bwd_sgd without lr and path (the sorted, deterministic path). */
+emb_status emb_bag_bwd_dense_grad(emb_plan* plan, void* grad_weights, const int64_t* indices,
+                                  const int64_t* offsets, int64_t N, int32_t B,
+                                  const float* per_sample_weights, const void* grad_output,
+                                  emb_pooling mode, void* stream);
+emb_status emb_nobag_bwd_dense_grad(emb_plan* plan, void* grad_weights, const int64_t* indices,
+                                    const int64_t* offsets, int64_t N, int32_t B,
+                                    const void* grad_output, void* stream);
+
 /* Unpooled backward + SGD: lookup l adds grad_output[l, :] (shape [N, D], every
  * table has the same D) to row indices[l] of its table, the table given by the
  * CSR offsets (B*T+1 entries; only table membership matters). There is no

@@ -88,7 +88,8 @@ struct emb_plan {
   uint32_t cap_long = 0, cap_slices = 0;
 
   uint32_t seq = 0;
-  int reduce_grid[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  int reduce_grid[3][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};  // [optimizer][value kind]
+  int64_t w_extent = 0;  // elements of the weights layout: max over t of offset + rows * D
   // Blocks that fit on the GPU at once: sort pass [large tiles][wide payload], k_runs [split].
   int pass_cap[2][2] = {{0, 0}, {0, 0}};
   int runs_cap[2] = {0, 0};
@@ -106,7 +107,8 @@ struct emb_plan {
 namespace {
 
 const void* reduce_fn(const emb_plan* p, int opt, int vk) {
-  const ReduceKey k{static_cast<int>(p->gdt), opt, vk, p->split[opt].kv, p->split[opt].segs.size() > 2};
+  const emb_plan::RowSplit& sp = p->split[opt == 1 ? 1 : 0];  // elementwise updates split rows like SGD
+  const ReduceKey k{static_cast<int>(p->gdt), opt, vk, sp.kv, sp.segs.size() > 2};
   static const void* (*const entry[3][3])(const ReduceKey&) = {
       {reduce_kernel_f32_f32, reduce_kernel_f32_f16, reduce_kernel_f32_bf16},
       {reduce_kernel_f16_f32, reduce_kernel_f16_f16, reduce_kernel_f16_bf16},
@@ -170,10 +172,13 @@ emb_status cuda_status(cudaError_t e) {
 #define EMB_CUDA(expr) EMB_TRY(cuda_status(expr))
 
 // Sorted path: linearise + sort + run-length + long partition + fused reduce/update.
+// opt: 0 SGD (or, with dense, the gradient stored to grad_out), 1 row-wise Adagrad,
+// 2 elementwise Adagrad.
 emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* momentum,
                       const int64_t* indices, const int64_t* offsets, int64_t N, int32_t B,
                       const float* psw, const void* grad, int mean, float lr, float eps,
-                      cudaStream_t s) {
+                      void* grad_out, int dense, cudaStream_t s) {
+  const int si = opt == 1 ? 1 : 0;  // row split of this optimizer
   const uint32_t epoch = ++p->seq * 8u;
   if (p->seq >= (1u << 28)) p->seq = 0;  // epochs stay distinct from the zero-initialised words
   const DecodeArgs d = decode_args(p, indices, offsets, psw, N, B, mean);
@@ -218,12 +223,12 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.run_key = p->run_key;
   ra.run_start = p->run_start;
   ra.thr = p->thr;
-  ra.ordered = (N + kRleTile - 1) / kRleTile <= p->runs_cap[opt];
+  ra.ordered = (N + kRleTile - 1) / kRleTile <= p->runs_cap[si];
   ra.long_ids = p->long_ids;
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
-  ra.seg_keys = p->split[opt].d_segkeys;
-  ra.S = (uint32_t)p->split[opt].segs.size() - 1;
+  ra.seg_keys = p->split[si].d_segkeys;
+  ra.S = (uint32_t)p->split[si].segs.size() - 1;
   ra.seg_runs = p->seg_runs;
   EMB_CUDA(launch_runs(ra, s, pdl));
   EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel (no event 4)
@@ -234,8 +239,8 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.run_key = p->run_key;
   r.run_start = p->run_start;
   r.seg_runs = p->seg_runs;
-  r.segs = p->split[opt].d_segs;
-  r.S = (uint32_t)p->split[opt].segs.size() - 1;
+  r.segs = p->split[si].d_segs;
+  r.S = (uint32_t)p->split[si].segs.size() - 1;
   r.longs = p->longs;
   r.partials = p->partials;
   r.done = p->done;
@@ -254,7 +259,9 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.eps = eps;
   r.thr = p->thr;
   r.min_slice = kMinSlice;
-  r.C = p->split[opt].C;
+  r.C = p->split[si].C;
+  r.grad_out = grad_out;
+  r.dense = dense;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
@@ -362,6 +369,9 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->hsc.resize(T + 1);
   p->Do.assign(D_offsets, D_offsets + T + 1);
   for (int32_t t = 0; t <= T; ++t) p->hsc[t] = (uint32_t)hash_size_cumsum[t];
+  for (int32_t t = 0; t < T; ++t)
+    p->w_extent = std::max<int64_t>(p->w_extent, weights_offsets[t] + (hash_size_cumsum[t + 1] - hash_size_cumsum[t]) *
+                                                                      (int64_t)(D_offsets[t + 1] - D_offsets[t]));
 
   DeviceGuard g(device);
   if (!g.ok) {
@@ -380,7 +390,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   int max_grid = 1;
   {
     cudaError_t e = cudaSuccess;
-    for (int opt = 0; opt < 2 && e == cudaSuccess; ++opt) {
+    for (int opt = 0; opt < 3 && e == cudaSuccess; ++opt) {
       for (int vk = 0; vk < 3 && e == cudaSuccess; ++vk) {
         const void* fn = reduce_fn(p, opt, vk);
         if (!fn) continue;
@@ -520,7 +530,8 @@ emb_status emb_bag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
   if (!g.ok) return EMB_ERR_CUDA;
   const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
   return run_sorted(p, 0, vk, weights, nullptr, indices, offsets, N, B, per_sample_weights,
-                    grad_output, mode == EMB_POOL_MEAN, lr, 0.0f, static_cast<cudaStream_t>(stream));
+                    grad_output, mode == EMB_POOL_MEAN, lr, 0.0f, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
 }
 
 emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* momentum,
@@ -541,7 +552,65 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* moment
   if (!g.ok) return EMB_ERR_CUDA;
   const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
   return run_sorted(p, 1, vk, weights, momentum, indices, offsets, N, B, per_sample_weights,
-                    grad_output, mode == EMB_POOL_MEAN, lr, eps, static_cast<cudaStream_t>(stream));
+                    grad_output, mode == EMB_POOL_MEAN, lr, eps, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+emb_status emb_bag_bwd_adagrad(emb_plan* p, void* weights, float* momentum, const int64_t* indices,
+                               const int64_t* offsets, int64_t N, int32_t B,
+                               const float* per_sample_weights, const void* grad_output,
+                               emb_pooling mode, float lr, float eps, void* stream) {
+  EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
+  if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
+  if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
+  if (N == 0) {
+    p->last_kind = 0;
+    return EMB_OK;
+  }
+  if (!momentum || !aligned(momentum, 16)) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
+  return run_sorted(p, 2, vk, weights, momentum, indices, offsets, N, B, per_sample_weights,
+                    grad_output, mode == EMB_POOL_MEAN, lr, eps, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+// Dense-gradient mode for pooled (vk from the pooling) or unpooled lookups.
+static emb_status dense_grad(emb_plan* p, void* grad_weights, const int64_t* indices,
+                      const int64_t* offsets, int64_t N, int32_t B, const float* psw,
+                      const void* grad_output, int vk, int mean, void* stream) {
+  if (!p || !grad_weights || !aligned(grad_weights, 4 * dtype_size(p->wdt))) return EMB_ERR_INVALID_ARG;
+  EMB_TRY(check_common(p, grad_weights, indices, offsets, N, B, grad_output));
+  if (psw && !aligned(psw, 4)) return EMB_ERR_INVALID_ARG;
+  DeviceGuard g(p->device);
+  if (!g.ok) return EMB_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EMB_CUDA(cudaMemsetAsync(grad_weights, 0, (size_t)p->w_extent * dtype_size(p->wdt), s));
+  if (N == 0) {
+    p->last_kind = 0;
+    p->last_stream = s;
+    return EMB_OK;
+  }
+  return run_sorted(p, 0, vk, grad_weights, nullptr, indices, offsets, N, B, psw, grad_output, mean,
+                    0.0f, 0.0f, grad_weights, 1, s);
+}
+
+emb_status emb_bag_bwd_dense_grad(emb_plan* p, void* grad_weights, const int64_t* indices,
+                                  const int64_t* offsets, int64_t N, int32_t B,
+                                  const float* per_sample_weights, const void* grad_output,
+                                  emb_pooling mode, void* stream) {
+  if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
+  const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
+  return dense_grad(p, grad_weights, indices, offsets, N, B, per_sample_weights, grad_output, vk,
+                    mode == EMB_POOL_MEAN, stream);
+}
+
+emb_status emb_nobag_bwd_dense_grad(emb_plan* p, void* grad_weights, const int64_t* indices,
+                                    const int64_t* offsets, int64_t N, int32_t B,
+                                    const void* grad_output, void* stream) {
+  if (p && !p->uniform_D) return EMB_ERR_INVALID_ARG;
+  return dense_grad(p, grad_weights, indices, offsets, N, B, nullptr, grad_output, VK_NOBAG, 0, stream);
 }
 
 emb_status emb_bag_fwd(emb_plan* p, const void* weights, const int64_t* indices,
@@ -633,7 +702,7 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
     return EMB_OK;
   }
   return run_sorted(p, 0, VK_NOBAG, weights, nullptr, indices, offsets, N, B, nullptr,
-                    grad_output, 0, lr, 0.0f, s);
+                    grad_output, 0, lr, 0.0f, nullptr, 0, s);
 }
 
 emb_status emb_plan_status(emb_plan* p) {

@@ -164,6 +164,8 @@ struct ReduceArgs {
   uint32_t T, B;
   int64_t grad_stride;      // elements per gradient row (sum of D, or D unpooled)
   float lr, eps;
+  void* grad_out;           // dense-gradient mode: weights-layout buffer that receives G
+  int dense;                // 1: store G (SGD kernels) instead of updating the weights
   uint32_t thr, C;
   uint32_t min_slice;       // fewest long-run lookups per warp slice
 };
@@ -523,7 +525,7 @@ size_t fwd_smem_bytes(int T, int S);
 // reduce_<weight>_<grad>.cu: one entry per (weight type, gradient type) pair.
 struct ReduceKey {
   int grad_dtype;   // 0 f32, 1 f16, 2 bf16
-  int optimizer;    // 0 SGD, 1 row-wise Adagrad
+  int optimizer;    // 0 SGD (or dense gradient), 1 row-wise Adagrad, 2 elementwise Adagrad
   int value_kind;   // ValueKind
   int kv;           // 1, 2, 4, 8 vectors of 4 per lane
   bool multi;       // tables of several team shapes

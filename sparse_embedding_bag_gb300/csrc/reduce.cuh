@@ -163,9 +163,11 @@ __device__ __forceinline__ void team_fold(float4 (&acc)[KV], uint32_t Lg, uint32
   }
 }
 
-template <typename emb_t, int KV>
+// The old weights of a row chunk (lane group 0 only; not read in dense-gradient mode).
+template <typename emb_t, int OPT, int KV>
 __device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs, bool active,
                                          uint32_t g, uint32_t li, float4 (&w)[KV]) {
+  if constexpr (OPT == 0) active = active && !a.dense;
   const emb_t* row = static_cast<const emb_t*>(a.weights) +
                      (active ? __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D : 0);
 #pragma unroll
@@ -178,6 +180,10 @@ __device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs
 
 // Optimizer update of the chunk held by lane group 0 of a team of Lt lanes
 // (acc = G, w = old weights, tl = lane in team). Warp-uniform shuffles.
+//   OPT 0: SGD w -= lr * G, or in dense-gradient mode G stored to grad_out;
+//   OPT 1: row-wise Adagrad (state per row);
+//   OPT 2: elementwise Adagrad (state per element, laid out like the weights):
+//          m += G^2, w -= lr * G / (sqrt(m) + eps).
 template <typename emb_t, int OPT, int KV>
 __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& rs, bool active,
                                            uint32_t g, uint32_t li, uint32_t tl, uint32_t Lt,
@@ -199,7 +205,38 @@ __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& 
     if (active && tl == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
   }
   if (!active || g != 0) return;
+  if constexpr (OPT == 0) {
+    if (a.dense) {  // the gradient itself, in the weights' type and layout
+      emb_t* grow = static_cast<emb_t*>(a.grad_out) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const uint32_t q = li + (k << rs.lg);
+        if (q < rs.cvec) Vec4<emb_t>::store(grow + (int64_t)(rs.cvec_off + q) * 4, acc[k]);
+      }
+      return;
+    }
+  }
   emb_t* row = static_cast<emb_t*>(a.weights) + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+  if constexpr (OPT == 2) {
+    float* mrow = a.momentum + __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const uint32_t q = li + (k << rs.lg);
+      if (q < rs.cvec) {
+        float4* mp = reinterpret_cast<float4*>(mrow + (int64_t)(rs.cvec_off + q) * 4);
+        float4 m = *mp;
+        m = make_float4(fmaf(acc[k].x, acc[k].x, m.x), fmaf(acc[k].y, acc[k].y, m.y),
+                        fmaf(acc[k].z, acc[k].z, m.z), fmaf(acc[k].w, acc[k].w, m.w));
+        *mp = m;
+        const float4 n = make_float4(fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.x) + a.eps), acc[k].x, w[k].x),
+                                     fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.y) + a.eps), acc[k].y, w[k].y),
+                                     fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.z) + a.eps), acc[k].z, w[k].z),
+                                     fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.w) + a.eps), acc[k].w, w[k].w));
+        Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + q) * 4, n);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const uint32_t q = li + (k << rs.lg);
@@ -436,14 +473,14 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
         team_gather<VK, grad_t, KV>(a, rs, jb, je, steps, Pg, g, li, acc);
         team_fold<KV>(acc, 1u << rs.lg, 32);
         if (whole) {  // long runs: the row is read after the gather (registers)
-          load_row<emb_t, KV>(a, rs, true, g, li, wv);
+          load_row<emb_t, OPT, KV>(a, rs, true, g, li, wv);
           if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
           update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
           continue;
         }
         // a piece of a run cut by slice ends
         if (!piece_arrive<KV>(a, rs, g, li, c * S1, sl.of(p0), sl.of(p1 - 1), s, acc)) continue;
-        load_row<emb_t, KV>(a, rs, true, g, li, wv);
+        load_row<emb_t, OPT, KV>(a, rs, true, g, li, wv);
         if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
         update_row<emb_t, OPT, KV>(a, rs, true, g, li, lane, 32, acc, wv, m_old);
       }
@@ -477,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
     const uint32_t Pt = Lt >> rs.lg;
     const uint32_t g = tl >> rs.lg, li = tl & ((1u << rs.lg) - 1);
     float4 wv[KV];
-    load_row<emb_t, KV>(a, rs, active, g, li, wv);
+    load_row<emb_t, OPT, KV>(a, rs, active, g, li, wv);
     float m_old = 0.f;
     if constexpr (OPT == 1) {
       if (active) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
@@ -564,6 +601,10 @@ const void* pick_vk(int opt, int vk, int kv) {
   } else if (opt == 1) {
     if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 1, VK_BAG, MULTI>(kv);
     if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 1, VK_BAG_SCALED, MULTI>(kv);
+  } else if (opt == 2) {
+    if (vk == VK_BAG) return pick_kv<emb_t, grad_t, 2, VK_BAG, MULTI>(kv);
+    if (vk == VK_BAG_SCALED) return pick_kv<emb_t, grad_t, 2, VK_BAG_SCALED, MULTI>(kv);
+    if (vk == VK_NOBAG) return pick_kv<emb_t, grad_t, 2, VK_NOBAG, MULTI>(kv);
   }
   return nullptr;
 }

@@ -29,7 +29,8 @@ EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_rowwise_adagrad",
            "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
            "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc",
-           "emb_bag_fwd")
+           "emb_bag_fwd", "emb_bag_bwd_adagrad", "emb_bag_bwd_dense_grad",
+           "emb_nobag_bwd_dense_grad")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +67,9 @@ def load(path: str = LIB_PATH):
             "emb_nobag_bwd_sgd_atomic_noalloc": [c_int, i32, vp, vp, i32, vp, vp, vp, i64, i32, vp,
                                                  c_int, f32, vp, vp],
             "emb_bag_fwd": [vp, vp, vp, vp, i64, i32, vp, c_int, vp, c_int, vp],
+            "emb_bag_bwd_adagrad": [vp, vp, vp, vp, vp, i64, i32, vp, vp, c_int, f32, f32, vp],
+            "emb_bag_bwd_dense_grad": [vp, vp, vp, vp, i64, i32, vp, vp, c_int, vp],
+            "emb_nobag_bwd_dense_grad": [vp, vp, vp, vp, i64, i32, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -154,6 +158,29 @@ def emb_nobag_bwd_sgd(plan, weights, indices, offsets, N, B, grad_output, lr,
     st = load().emb_nobag_bwd_sgd(plan, _ptr(weights), _ptr(indices), _ptr(offsets), int(N),
                                   int(B), _ptr(grad_output), float(lr), int(path), _stream(stream))
     return _check(st, "emb_nobag_bwd_sgd")
+
+
+def emb_bag_bwd_adagrad(plan, weights, momentum, indices, offsets, N, B, per_sample_weights,
+                        grad_output, mode, lr, eps, stream=None):
+    st = load().emb_bag_bwd_adagrad(plan, _ptr(weights), _ptr(momentum), _ptr(indices),
+                                    _ptr(offsets), int(N), int(B), _ptr(per_sample_weights),
+                                    _ptr(grad_output), int(mode), float(lr), float(eps),
+                                    _stream(stream))
+    return _check(st, "emb_bag_bwd_adagrad")
+
+
+def emb_bag_bwd_dense_grad(plan, grad_weights, indices, offsets, N, B, per_sample_weights,
+                           grad_output, mode, stream=None):
+    st = load().emb_bag_bwd_dense_grad(plan, _ptr(grad_weights), _ptr(indices), _ptr(offsets),
+                                       int(N), int(B), _ptr(per_sample_weights),
+                                       _ptr(grad_output), int(mode), _stream(stream))
+    return _check(st, "emb_bag_bwd_dense_grad")
+
+
+def emb_nobag_bwd_dense_grad(plan, grad_weights, indices, offsets, N, B, grad_output, stream=None):
+    st = load().emb_nobag_bwd_dense_grad(plan, _ptr(grad_weights), _ptr(indices), _ptr(offsets),
+                                         int(N), int(B), _ptr(grad_output), _stream(stream))
+    return _check(st, "emb_nobag_bwd_dense_grad")
 
 
 def emb_bag_fwd(plan, weights, indices, offsets, N, B, per_sample_weights, mode, output,
