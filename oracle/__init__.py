@@ -74,7 +74,14 @@ def _load():
                                              i32, vp, vp, vp]
             lib.oracle_apply_row.argtypes = [i32, i32, vp, i64, i32, vp, vp, f64, f64]
             lib.oracle_backward.argtypes = [i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, vp,
-                                            i32, i32, i32, vp, i32, f64, f64]
+                                            i32, i32, i32, vp, i32, f64, f64, i32, ctypes.c_uint64,
+                                            ctypes.c_uint64]
+            lib.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_sr_bf16.argtypes = [ctypes.c_float, ctypes.c_uint32]
+            lib.oracle_sr_bf16.restype = ctypes.c_uint16
+            lib.oracle_sr_half.argtypes = [ctypes.c_float, ctypes.c_uint32]
+            lib.oracle_sr_half.restype = ctypes.c_uint16
             lib.oracle_forward.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp, vp, i64, vp, i32,
                                            i32, vp]
             lib.oracle_dense_grad.argtypes = [i32, i32, vp, vp, vp, i64, i32, vp, vp, vp, i64, vp,
@@ -189,11 +196,14 @@ def apply_row(optimizer, weights, row_offset, D, g, momentum=None, momentum_inde
 
 def backward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices, offsets,
              grad_output, *, optimizer, lr, eps=0.0, momentum=None, momentum_offsets=None,
-             per_sample_weights=None, mean=False, nobag=False, grad_dtype=None):
+             per_sample_weights=None, mean=False, nobag=False, grad_dtype=None,
+             stochastic_rounding=None):
     """Full backward + in-place optimizer on numpy `weights` (and `momentum`).
 
     `weights` is float32, float16, or uint16 holding bfloat16 bits; `lr` and
     `eps` should be the exact fp32 values the device path receives.
+    stochastic_rounding: None (round to nearest even) or (seed, call) for
+    stochastic rounding of fp16 / bf16 weight stores.
     """
     hsc, Do = _c(hash_size_cumsum, np.int64), _c(D_offsets, np.int32)
     wo, mo = _c(weights_offsets, np.int64), _c(momentum_offsets, np.int64)
@@ -207,7 +217,8 @@ def backward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indice
     _check(_load().oracle_backward(T, B, _p(hsc), _p(Do), _p(wo), _p(mo), dtype_code(weights),
                                    _p(weights), _p(momentum), _p(idx), _p(off), idx.size, _p(psw),
                                    int(bool(mean)), int(bool(nobag)), gcode, _p(g), optimizer,
-                                   float(lr), float(eps)))
+                                   float(lr), float(eps), int(stochastic_rounding is not None),
+                                   *(stochastic_rounding or (0, 0))))
 
 
 def dense_grad(T, B, hash_size_cumsum, D_offsets, weights_offsets, extent, indices, offsets,
@@ -241,6 +252,22 @@ def forward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices
                                   _p(idx), _p(off), idx.size, _p(psw), int(bool(mean)), out_dtype,
                                   _p(out)))
     return out
+
+
+def philox4x32_10(ctr, key):
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    _load().oracle_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def sr_bf16_bits(x: float, r: int) -> int:
+    return int(_load().oracle_sr_bf16(float(x), int(r)))
+
+
+def sr_half_bits(x: float, r: int) -> int:
+    return int(_load().oracle_sr_half(float(x), int(r)))
 
 
 def double_to_half_bits(x: float) -> int:

@@ -115,6 +115,53 @@ uint16_t double_to_bf16(double x) {
   return sign | static_cast<uint16_t>(((E + 127) << 7) | (static_cast<int>(r) - 128));
 }
 
+// ---- stochastic rounding of fp16 / bf16 stores.
+// Random words: Philox4x32-10, written from its published definition (Salmon,
+// Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+// ten rounds of two 32x32->64 multiplies by M0, M1 on a 4-word counter, with the
+// 2-word key bumped by the Weyl constants W0, W1 between rounds.
+void philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k[2] = {key_in[0], key_in[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += W0;
+      k[1] += W1;
+    }
+    const uint64_t p0 = M0 * c[0], p1 = M1 * c[2];
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+    const uint32_t n[4] = {hi1 ^ c[1] ^ k[0], lo1, hi0 ^ c[3] ^ k[1], lo0};
+    for (int j = 0; j < 4; ++j) c[j] = n[j];
+  }
+  for (int j = 0; j < 4; ++j) out[j] = c[j];
+}
+
+// fp32 x to bf16 with probability of rounding away from zero equal to the
+// dropped fraction: add 16 random bits to the dropped low half, truncate.
+uint16_t sr_bf16(float x, uint32_t r) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return static_cast<uint16_t>((u >> 16) | ((u & 0xFFFF) ? 0x40 : 0));
+  return static_cast<uint16_t>((u + (r & 0xFFFFu)) >> 16);
+}
+
+// fp32 x to fp16: the neighbour toward zero, moved one ulp away from zero with
+// probability (|x| - |lo|) / ulp, compared on 24 random bits (both exact in fp32).
+uint16_t sr_half(float x, uint32_t r) {
+  uint16_t lo = double_to_half(static_cast<double>(x));  // nearest; step toward zero if past x
+  if (std::fabs(half_to_double(lo)) > std::fabs(static_cast<double>(x))) lo = static_cast<uint16_t>(lo - 1);
+  if ((lo & 0x7C00) == 0x7C00) return lo;  // inf / nan
+  const uint16_t hi = static_cast<uint16_t>(lo + 1);
+  const float a = std::fabs(static_cast<float>(half_to_double(lo)));
+  const float b = std::fabs(static_cast<float>(half_to_double(hi)));
+  const float frac = (std::fabs(x) - a) / (b - a);
+  const uint32_t thresh = static_cast<uint32_t>(frac * 16777216.0f);
+  return (r >> 8) < thresh ? hi : lo;
+}
+
 double load_elem(const void* base, int dtype, int64_t i) {
   switch (dtype) {
     case DT_F32: return static_cast<double>(static_cast<const float*>(base)[i]);
@@ -130,6 +177,36 @@ void store_elem(void* base, int dtype, int64_t i, double v) {
     default: static_cast<uint16_t*>(base)[i] = double_to_bf16(v); break;
   }
 }
+
+// A 16-bit store with stochastic rounding of v rounded first to fp32 (the type
+// the update is computed in on the device); fp32 stores are plain.
+void store_elem_sr(void* base, int dtype, int64_t i, double v, uint32_t r) {
+  const float f = static_cast<float>(v);
+  switch (dtype) {
+    case DT_F32: static_cast<float*>(base)[i] = f; break;
+    case DT_F16: static_cast<uint16_t*>(base)[i] = sr_half(f, r); break;
+    default: static_cast<uint16_t*>(base)[i] = sr_bf16(f, r); break;
+  }
+}
+
+// Random word of element d of the row with linear index `key` in update call
+// `call`: word d % 4 of Philox4x32-10 at counter (key, d / 4, call_lo, call_hi)
+// under the 64-bit seed.
+uint32_t sr_word(uint64_t seed, uint64_t call, int64_t key, int32_t d) {
+  const uint32_t ctr[4] = {static_cast<uint32_t>(key), static_cast<uint32_t>(d / 4),
+                           static_cast<uint32_t>(call), static_cast<uint32_t>(call >> 32)};
+  const uint32_t k[2] = {static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+  uint32_t out[4];
+  philox4x32_10(ctr, k, out);
+  return out[d % 4];
+}
+
+// Stochastic rounding of the weight stores of one call (or off).
+struct Rounding {
+  int on = 0;
+  uint64_t seed = 0, call = 0;
+  int64_t key = 0;  // linear index of the row being stored
+};
 
 struct Pair {
   int64_t key;  // linear index
@@ -298,14 +375,26 @@ int oracle_row_grads(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_
 //   optimizer 0 = SGD, 1 = row-wise Adagrad, 2 = elementwise Adagrad
 //   ("tt_embeddings_cuda.cu", update_tt_cores_adagrad_kernel: per element
 //   m <- m + g^2, w <- w - lr * g / (sqrt(m) + eps)).
+int apply_row_impl(int32_t optimizer, int32_t weight_dtype, void* weights, int64_t row_offset,
+                   int32_t D, const double* g, float* m, double lr, double eps, const Rounding& rnd);
+
 int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int64_t row_offset,
                      int32_t D, const double* g, float* m, double lr, double eps) {
+  return apply_row_impl(optimizer, weight_dtype, weights, row_offset, D, g, m, lr, eps, Rounding());
+}
+
+int apply_row_impl(int32_t optimizer, int32_t weight_dtype, void* weights, int64_t row_offset,
+                   int32_t D, const double* g, float* m, double lr, double eps, const Rounding& rnd) {
+  auto store = [&](int64_t i, int32_t d, double v) {
+    if (rnd.on) store_elem_sr(weights, weight_dtype, i, v, sr_word(rnd.seed, rnd.call, rnd.key, d));
+    else store_elem(weights, weight_dtype, i, v);
+  };
   if (optimizer == 2) {
     if (!m) return ERR_INVALID_ARG;
     for (int32_t d = 0; d < D; ++d) {
       const double m_new = static_cast<double>(m[d]) + g[d] * g[d];
       const double w = load_elem(weights, weight_dtype, row_offset + d);
-      store_elem(weights, weight_dtype, row_offset + d, w - lr * g[d] / (std::sqrt(m_new) + eps));
+      store(row_offset + d, d, w - lr * g[d] / (std::sqrt(m_new) + eps));
       m[d] = static_cast<float>(m_new);
     }
     return OK;
@@ -313,7 +402,7 @@ int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int
   if (optimizer == 0) {
     for (int32_t d = 0; d < D; ++d) {
       const double w = load_elem(weights, weight_dtype, row_offset + d);
-      store_elem(weights, weight_dtype, row_offset + d, w - lr * g[d]);
+      store(row_offset + d, d, w - lr * g[d]);
     }
     return OK;
   }
@@ -324,7 +413,7 @@ int oracle_apply_row(int32_t optimizer, int32_t weight_dtype, void* weights, int
   const double mult = lr / (std::sqrt(m_new) + eps);
   for (int32_t d = 0; d < D; ++d) {
     const double w = load_elem(weights, weight_dtype, row_offset + d);
-    store_elem(weights, weight_dtype, row_offset + d, w - mult * g[d]);
+    store(row_offset + d, d, w - mult * g[d]);
   }
   *m = static_cast<float>(m_new);
   return OK;
@@ -342,7 +431,7 @@ int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_o
                     const int64_t* indices, const int64_t* offsets, int64_t N,
                     const float* per_sample_weights, int32_t mean_pooling, int32_t nobag,
                     int32_t grad_dtype, const void* grad_output, int32_t optimizer, double lr,
-                    double eps) {
+                    double eps, int32_t stochastic_rounding, uint64_t seed, uint64_t call) {
   if (T <= 0 || B <= 0) return ERR_INVALID_ARG;
   if (N == 0) return OK;
   int32_t Dmax = 0;
@@ -365,8 +454,13 @@ int oracle_backward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_o
     } else if (optimizer == 2) {
       m = momentum + weights_offsets[t] + idx * D;
     }
-    const int st2 = oracle_apply_row(optimizer, weight_dtype, weights, weights_offsets[t] + idx * D,
-                                     D, G.data() + r * static_cast<int64_t>(Dmax), m, lr, eps);
+    Rounding rnd;
+    rnd.on = stochastic_rounding;
+    rnd.seed = seed;
+    rnd.call = call;
+    rnd.key = keys[r];
+    const int st2 = apply_row_impl(optimizer, weight_dtype, weights, weights_offsets[t] + idx * D, D,
+                                   G.data() + r * static_cast<int64_t>(Dmax), m, lr, eps, rnd);
     if (st2 != OK) return st2;
   }
   return OK;
@@ -446,6 +540,13 @@ int oracle_forward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_of
   }
   return OK;
 }
+
+// Stochastic rounding pieces, exported for the pin tests.
+void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) {
+  philox4x32_10(ctr, key, out);
+}
+uint16_t oracle_sr_bf16(float x, uint32_t r) { return sr_bf16(x, r); }
+uint16_t oracle_sr_half(float x, uint32_t r) { return sr_half(x, r); }
 
 // Storage conversions, exported for the pin tests.
 uint16_t oracle_double_to_half(double x) { return double_to_half(x); }
