@@ -72,6 +72,22 @@ typedef enum { EMB_NOBAG_AUTO = 0, EMB_NOBAG_SORTED = 1, EMB_NOBAG_ATOMIC = 2 } 
 /* Launch the kernels of a call as plain stream-ordered launches instead of
  * programmatic dependent launches (for A/B timing; results are identical). */
 #define EMB_FLAG_NO_PDL 0x2u
+/* Stochastic rounding of fp16 / bf16 weight stores ("embedding_backward_split_
+ * template.cu", the stochastic_rounding argument of the per-row kernels and
+ * their Philox-seeded 16-bit stores): an update is rounded to one of its two
+ * representable neighbours, away from zero with probability equal to the
+ * fraction of an ulp it lies past the one toward zero (unbiased in expectation). Applies to the SGD and Adagrad updates of plans
+ * with 16-bit weights (fp32 weights and the dense-gradient mode store as usual).
+ * Element d of the row with linear index K, in the update call numbered c, draws
+ * word d mod 4 of Philox4x32-10 (Salmon et al., SC 2011) at counter
+ * (K, d / 4, c mod 2^32, c / 2^32) under the key (seed mod 2^32, seed / 2^32).
+ * bf16: the 16 low bits of the word are added to the fp32 pattern, then it is
+ * truncated; fp16: the neighbour away from zero is taken iff (word >> 8) <
+ * floor(fraction * 2^24). The call number starts at 0; each SGD or Adagrad
+ * call with N > 0 on a plan with 16-bit weights takes the next one;
+ * emb_plan_set_rounding sets seed and number.
+ * A call captured in a CUDA graph keeps the number it was captured with. */
+#define EMB_FLAG_STOCHASTIC_ROUNDING 0x4u
 /* Test only: every block that would wait on another one gives up at once and
  * reports EMB_ERR_TIMEOUT, exercising the error path without a real stall. */
 #define EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u
@@ -105,6 +121,13 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
                         const int64_t* momentum_offsets, emb_dtype weight_dtype,
                         emb_dtype grad_dtype, int64_t max_N, int32_t max_B,
                         int32_t max_segment_length_per_warp, uint32_t flags);
+
+/* Stochastic rounding state of the plan: `seed` keys the random words and
+ * `next_call` is the call number the next update call uses (see
+ * EMB_FLAG_STOCHASTIC_ROUNDING). Host-side only; no synchronisation.
+ * emb_plan_get_rounding reads both back (either pointer may be NULL). */
+emb_status emb_plan_set_rounding(emb_plan* plan, uint64_t seed, uint64_t next_call);
+emb_status emb_plan_get_rounding(const emb_plan* plan, uint64_t* seed, uint64_t* next_call);
 
 /* Frees the plan and its scratch (synchronises the device). NULL is accepted. */
 emb_status emb_plan_destroy(emb_plan* plan);

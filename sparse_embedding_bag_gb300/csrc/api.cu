@@ -51,6 +51,7 @@ struct emb_plan {
   int32_t max_B = 0;
   uint32_t thr = 32;
   uint32_t flags = 0;
+  uint64_t sr_seed = 0, sr_call = 0;  // stochastic rounding: Philox key, next call number
   int max_D = 0;
   bool uniform_D = true;
   // How the reduce splits rows, per optimizer (0 SGD, 1 row-wise Adagrad).
@@ -262,6 +263,14 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.C = p->split[si].C;
   r.grad_out = grad_out;
   r.dense = dense;
+  r.sr = (p->flags & EMB_FLAG_STOCHASTIC_ROUNDING) && !dense && p->wdt != EMB_F32;
+  if (r.sr) {
+    const uint64_t call = p->sr_call++;
+    r.seed_lo = (uint32_t)p->sr_seed;
+    r.seed_hi = (uint32_t)(p->sr_seed >> 32);
+    r.call_lo = (uint32_t)call;
+    r.call_hi = (uint32_t)(call >> 32);
+  }
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
@@ -703,6 +712,20 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
   }
   return run_sorted(p, 0, VK_NOBAG, weights, nullptr, indices, offsets, N, B, nullptr,
                     grad_output, 0, lr, 0.0f, nullptr, 0, s);
+}
+
+emb_status emb_plan_set_rounding(emb_plan* p, uint64_t seed, uint64_t next_call) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  p->sr_seed = seed;
+  p->sr_call = next_call;
+  return EMB_OK;
+}
+
+emb_status emb_plan_get_rounding(const emb_plan* p, uint64_t* seed, uint64_t* next_call) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  if (seed) *seed = p->sr_seed;
+  if (next_call) *next_call = p->sr_call;
+  return EMB_OK;
 }
 
 emb_status emb_plan_status(emb_plan* p) {

@@ -166,6 +166,8 @@ struct ReduceArgs {
   float lr, eps;
   void* grad_out;           // dense-gradient mode: weights-layout buffer that receives G
   int dense;                // 1: store G (SGD kernels) instead of updating the weights
+  int sr;                   // 1: stochastic rounding of fp16 / bf16 weight stores
+  uint32_t seed_lo, seed_hi, call_lo, call_hi;  // its random words: Philox key and call
   uint32_t thr, C;
   uint32_t min_slice;       // fewest long-run lookups per warp slice
 };
@@ -417,6 +419,46 @@ __device__ __forceinline__ uint32_t div_by_B(uint32_t bt, uint32_t B, float invB
   return q;
 }
 
+// ---- stochastic rounding of fp16 / bf16 stores.
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC 2011): ten rounds of two 32x32->64 multiplies by M0, M1 on a
+// 4-word counter, the 2-word key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+    const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// fp32 x to bf16 bits, rounding away from zero with probability equal to the
+// dropped fraction: 16 random bits added to the dropped half, then truncation.
+__device__ __forceinline__ uint16_t sr_bf16(float x, uint32_t r) {
+  const uint32_t u = __float_as_uint(x);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
+  return (uint16_t)((u + (r & 0xFFFFu)) >> 16);
+}
+
+// fp32 x to fp16 bits: the neighbour toward zero, moved one ulp away from zero
+// with probability (|x| - |lo|) / ulp, compared on 24 random bits (exact in fp32).
+__device__ __forceinline__ uint16_t sr_half(float x, uint32_t r) {
+  const __half h = __float2half_rz(x);
+  const uint16_t lo = *reinterpret_cast<const uint16_t*>(&h);
+  if ((lo & 0x7C00u) == 0x7C00u) return lo;  // inf / nan
+  const uint16_t hi = (uint16_t)(lo + 1);
+  const float a = fabsf(__half2float(h));
+  const float b = fabsf(__half2float(*reinterpret_cast<const __half*>(&hi)));
+  const float frac = __fdiv_rn(fabsf(x) - a, b - a);
+  return (r >> 8) < (uint32_t)(frac * 16777216.0f) ? hi : lo;
+}
+
 // ---- 4-element vector loads/stores of the storage types, as fp32.
 
 template <typename T>
@@ -433,6 +475,7 @@ struct Vec4<float> {
   __device__ __forceinline__ static float4 load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
   __device__ __forceinline__ static float4 load_plain(const float* p) { return *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+  __device__ __forceinline__ static void store_sr(float* p, float4 v, uint4) { store(p, v); }
 };
 
 template <>
@@ -456,6 +499,12 @@ struct Vec4<__half> {
     u.y = *reinterpret_cast<const uint32_t*>(&b);
     *reinterpret_cast<uint2*>(p) = u;
   }
+  __device__ __forceinline__ static void store_sr(__half* p, float4 v, uint4 r) {
+    uint2 u;
+    u.x = (uint32_t)sr_half(v.x, r.x) | ((uint32_t)sr_half(v.y, r.y) << 16);
+    u.y = (uint32_t)sr_half(v.z, r.z) | ((uint32_t)sr_half(v.w, r.w) << 16);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
 };
 
 template <>
@@ -476,6 +525,12 @@ struct Vec4<__nv_bfloat16> {
     uint2 u;
     u.x = *reinterpret_cast<const uint32_t*>(&a);
     u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+  __device__ __forceinline__ static void store_sr(__nv_bfloat16* p, float4 v, uint4 r) {
+    uint2 u;
+    u.x = (uint32_t)sr_bf16(v.x, r.x) | ((uint32_t)sr_bf16(v.y, r.y) << 16);
+    u.y = (uint32_t)sr_bf16(v.z, r.z) | ((uint32_t)sr_bf16(v.w, r.w) << 16);
     *reinterpret_cast<uint2*>(p) = u;
   }
 };

@@ -178,6 +178,23 @@ __device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs
   }
 }
 
+// Store of updated weights: vector v (row-relative) of the row of rs. fp16 / bf16
+// rows take stochastic rounding when the call asks for it; the four random
+// words of the vector are Philox4x32-10 of the counter (linear row index, v,
+// call number) under the key (seed), one word per element.
+template <typename emb_t>
+__device__ __forceinline__ void store_weights(const ReduceArgs& a, const RowShape& rs, emb_t* p,
+                                              uint32_t v, float4 n) {
+  if constexpr (sizeof(emb_t) == 2) {
+    if (a.sr) {
+      const uint32_t key = __ldg(&a.hsc[rs.t]) + (uint32_t)rs.idx;
+      Vec4<emb_t>::store_sr(p, n, philox4x32_10(make_uint4(key, v, a.call_lo, a.call_hi), a.seed_lo, a.seed_hi));
+      return;
+    }
+  }
+  Vec4<emb_t>::store(p, n);
+}
+
 // Optimizer update of the chunk held by lane group 0 of a team of Lt lanes
 // (acc = G, w = old weights, tl = lane in team). Warp-uniform shuffles.
 //   OPT 0: SGD w -= lr * G, or in dense-gradient mode G stored to grad_out;
@@ -232,7 +249,7 @@ __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& 
                                      fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.y) + a.eps), acc[k].y, w[k].y),
                                      fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.z) + a.eps), acc[k].z, w[k].z),
                                      fmaf(-__fdiv_rn(a.lr, __fsqrt_rn(m.w) + a.eps), acc[k].w, w[k].w));
-        Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + q) * 4, n);
+        store_weights<emb_t>(a, rs, row + (int64_t)(rs.cvec_off + q) * 4, rs.cvec_off + q, n);
       }
     }
     return;
@@ -243,7 +260,7 @@ __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& 
     if (q < rs.cvec) {
       const float4 n = make_float4(fmaf(-mult, acc[k].x, w[k].x), fmaf(-mult, acc[k].y, w[k].y),
                                    fmaf(-mult, acc[k].z, w[k].z), fmaf(-mult, acc[k].w, w[k].w));
-      Vec4<emb_t>::store(row + (int64_t)(rs.cvec_off + q) * 4, n);
+      store_weights<emb_t>(a, rs, row + (int64_t)(rs.cvec_off + q) * 4, rs.cvec_off + q, n);
     }
   }
 }

@@ -23,6 +23,7 @@ EMB_POOL_SUM, EMB_POOL_MEAN = 0, 1
 EMB_NOBAG_AUTO, EMB_NOBAG_SORTED, EMB_NOBAG_ATOMIC = 0, 1, 2
 EMB_FLAG_CHECK_INDICES = 0x1
 EMB_FLAG_NO_PDL = 0x2
+EMB_FLAG_STOCHASTIC_ROUNDING = 0x4
 EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 
 # Every symbol include/embbwd.h declares (checked by the tests against the header).
@@ -30,7 +31,7 @@ EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_r
            "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
            "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc",
            "emb_bag_fwd", "emb_bag_bwd_adagrad", "emb_bag_bwd_dense_grad",
-           "emb_nobag_bwd_dense_grad")
+           "emb_nobag_bwd_dense_grad", "emb_plan_set_rounding", "emb_plan_get_rounding")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,8 @@ def load(path: str = LIB_PATH):
             "emb_bag_bwd_adagrad": [vp, vp, vp, vp, vp, i64, i32, vp, vp, c_int, f32, f32, vp],
             "emb_bag_bwd_dense_grad": [vp, vp, vp, vp, i64, i32, vp, vp, c_int, vp],
             "emb_nobag_bwd_dense_grad": [vp, vp, vp, vp, i64, i32, vp, vp],
+            "emb_plan_set_rounding": [vp, ctypes.c_uint64, ctypes.c_uint64],
+            "emb_plan_get_rounding": [vp, vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -216,6 +219,20 @@ def emb_plan_debug_runs(plan, capacity):
 
 def emb_plan_set_profiling(plan, enable):
     return _check(load().emb_plan_set_profiling(plan, int(bool(enable))), "emb_plan_set_profiling")
+
+
+def emb_plan_set_rounding(plan, seed, next_call=0):
+    return _check(load().emb_plan_set_rounding(plan, int(seed) & (2 ** 64 - 1),
+                                               int(next_call) & (2 ** 64 - 1)),
+                  "emb_plan_set_rounding")
+
+
+def emb_plan_get_rounding(plan):
+    """(seed, next call number) of the plan's stochastic rounding."""
+    out = np.zeros(2, np.uint64)
+    _check(load().emb_plan_get_rounding(plan, out.ctypes.data, out.ctypes.data + 8),
+           "emb_plan_get_rounding")
+    return int(out[0]), int(out[1])
 
 
 def emb_plan_stage_ms(plan, n=5):
