@@ -86,9 +86,12 @@ def _load():
                                            i32, vp]
             lib.oracle_dense_grad.argtypes = [i32, i32, vp, vp, vp, i64, i32, vp, vp, vp, i64, vp,
                                               i32, i32, i32, vp]
+            lib.oracle_bucketize.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp,
+                                             vp]
+            lib.oracle_merge.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp]
             for name in ("oracle_sorted_pairs", "oracle_runs", "oracle_row_grads",
                          "oracle_apply_row", "oracle_backward", "oracle_forward",
-                         "oracle_dense_grad"):
+                         "oracle_dense_grad", "oracle_bucketize", "oracle_merge"):
                 getattr(lib, name).restype = ctypes.c_int
             lib.oracle_double_to_half.argtypes = [f64]
             lib.oracle_double_to_half.restype = ctypes.c_uint16
@@ -252,6 +255,37 @@ def forward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices
                                   _p(idx), _p(off), idx.size, _p(psw), int(bool(mean)), out_dtype,
                                   _p(out)))
     return out
+
+
+def bucketize(T, B, row_bounds, indices, offsets, *, per_sample_weights=None, mean=False):
+    """A rank's batch split by the owner of each lookup's row (row_bounds [T, W+1]).
+
+    Returns (send_offsets [W, T*B+1], send_indices, send_scales, send_counts [W]):
+    owner r's lookups are send_indices[sum(send_counts[:r]) : ...], rows relative
+    to r's range, scales = per-sample weight (1 if none) / L under mean pooling."""
+    rb = _c(row_bounds, np.int64)
+    W = rb.shape[1] - 1
+    idx, off = _c(indices, np.int64), _c(offsets, np.int64)
+    psw = _c(per_sample_weights, np.float32)
+    so = np.zeros((W, T * B + 1), np.int64)
+    si = np.zeros(idx.size, np.int64)
+    ss = np.zeros(idx.size, np.float32)
+    sc = np.zeros(W, np.int64)
+    _check(_load().oracle_bucketize(T, B, W, _p(rb), _p(idx), _p(off), idx.size, _p(psw),
+                                    int(bool(mean)), _p(so), _p(si), _p(ss), _p(sc)))
+    return so, si, ss, sc
+
+
+def merge(T, B, W, recv_offsets, recv_indices, recv_scales):
+    """The owner's batch after the exchange: CSR over T tables x W*B bags
+    (bag s*B + b = source s's bag b), with its indices and scales."""
+    ro = _c(recv_offsets, np.int64).reshape(W, T * B + 1)
+    ri, rs = _c(recv_indices, np.int64), _c(recv_scales, np.float32)
+    mo = np.zeros(T * W * B + 1, np.int64)
+    mi = np.zeros(ri.size, np.int64)
+    ms = np.zeros(ri.size, np.float32)
+    _check(_load().oracle_merge(T, B, W, _p(ro), _p(ri), _p(rs), _p(mo), _p(mi), _p(ms)))
+    return mo, mi, ms
 
 
 def philox4x32_10(ctr, key):

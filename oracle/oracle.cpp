@@ -31,6 +31,8 @@
 //   6. round w to its storage type (round to nearest, ties to even) and m to fp32.
 //
 // The forward pooled lookup (oracle_forward) is the adjoint of steps 1-4.
+// Row-wise sharding (oracle_bucketize, oracle_merge) is the exchange step of a
+// deployment over several ranks: each lookup moved to the rank owning its row.
 //
 // Every function here is pinned by tests/test_oracle_*.py against brute force
 // (a dense one-hot matrix product), closed forms and invariants.
@@ -538,6 +540,110 @@ int oracle_forward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_of
     }
     for (int32_t d = 0; d < D; ++d) store_elem(out, out_dtype, b * row_stride + D_offsets[t] + d, acc[d]);
   }
+  return OK;
+}
+
+// ---- row-wise sharding with an exchange step.
+// W ranks each own a contiguous row range of every table: rank r holds rows
+// [row_bounds[t*(W+1) + r], row_bounds[t*(W+1) + r + 1]) of table t, the
+// vocabulary sharding of "Function _embedding_bwd_kernel" (tinygrad: a device
+// owns one slice of the rows, lookups outside it add nothing there). Under
+// data-parallel batches every rank sends each of its lookups to the rank that
+// owns its row (an all-to-all) and gathers the gradient rows of all ranks' bags
+// (an all-gather); each owner then runs the backward on the lookups it received,
+// the batches of all ranks side by side, and updates its rows only.
+
+// The bucketing a rank does before the exchange: its batch (T tables x B bags,
+// CSR offsets, table-major) split by owner. Owner r's part lists, bag by bag
+// and in lookup order, the row relative to r's range and the lookup's scale:
+// its per-sample weight (1 if none) and, under mean pooling, divided by the
+// length L of its whole bag (both in fp32, one rounding, as the backward scales
+// a lookup), so that the owner can run the weighted-sum backward on it.
+//   send_offsets [W][T*B+1]: owner r's bag offsets, counted from its first lookup;
+//   send_indices, send_scales [N]: owner 0's lookups first, then owner 1's, ...;
+//   send_counts [W]: lookups per owner.
+int oracle_bucketize(int32_t T, int32_t B, int32_t W, const int64_t* row_bounds,
+                     const int64_t* indices, const int64_t* offsets, int64_t N,
+                     const float* per_sample_weights, int32_t mean_pooling,
+                     int64_t* send_offsets, int64_t* send_indices, float* send_scales,
+                     int64_t* send_counts) {
+  if (T <= 0 || B <= 0 || W <= 0) return ERR_INVALID_ARG;
+  const int64_t BT = static_cast<int64_t>(T) * B;
+  for (int32_t t = 0; t < T; ++t) {
+    const int64_t* rb = row_bounds + static_cast<int64_t>(t) * (W + 1);
+    if (rb[0] != 0) return ERR_INVALID_ARG;
+    for (int32_t r = 0; r < W; ++r)
+      if (rb[r + 1] < rb[r]) return ERR_INVALID_ARG;
+  }
+  if (offsets[0] != 0 || offsets[BT] != N) return ERR_INVALID_ARG;
+  for (int64_t bt = 0; bt < BT; ++bt)
+    if (offsets[bt + 1] < offsets[bt]) return ERR_INVALID_ARG;
+  std::vector<std::vector<int64_t>> idx(static_cast<size_t>(W));
+  std::vector<std::vector<float>> scale(static_cast<size_t>(W));
+  for (int32_t r = 0; r < W; ++r) send_offsets[static_cast<int64_t>(r) * (BT + 1)] = 0;
+  for (int64_t bt = 0; bt < BT; ++bt) {
+    const int32_t t = static_cast<int32_t>(bt / B);
+    const int64_t* rb = row_bounds + static_cast<int64_t>(t) * (W + 1);
+    const int64_t L = offsets[bt + 1] - offsets[bt];
+    for (int64_t i = offsets[bt]; i < offsets[bt + 1]; ++i) {
+      const int64_t row = indices[i];
+      if (row < 0 || row >= rb[W]) return ERR_INDEX_OUT_OF_RANGE;
+      int32_t r = 0;
+      while (!(row >= rb[r] && row < rb[r + 1])) ++r;  // empty ranges never match
+      float s = per_sample_weights ? per_sample_weights[i] : 1.0f;
+      // fp32 quotient, rounded once: the double quotient of two floats rounds to
+      // the same fp32 value (53 >= 2 * 24 + 2 bits)
+      if (mean_pooling) s = static_cast<float>(static_cast<double>(s) / static_cast<double>(static_cast<float>(L)));
+      idx[r].push_back(row - rb[r]);
+      scale[r].push_back(s);
+    }
+    for (int32_t r = 0; r < W; ++r)
+      send_offsets[static_cast<int64_t>(r) * (BT + 1) + bt + 1] = static_cast<int64_t>(idx[r].size());
+  }
+  int64_t pos = 0;
+  for (int32_t r = 0; r < W; ++r) {
+    send_counts[r] = static_cast<int64_t>(idx[r].size());
+    for (size_t k = 0; k < idx[r].size(); ++k, ++pos) {
+      send_indices[pos] = idx[r][k];
+      send_scales[pos] = scale[r][k];
+    }
+  }
+  return OK;
+}
+
+// The owner's side after the exchange: the parts received from the W sources
+// (source s's bag offsets recv_offsets[s][T*B+1], counted from its first lookup;
+// the lookups of all sources concatenated in source order) laid out as one batch
+// of W*B bags per table, table-major, bag s*B + b of table t holding source s's
+// bag (t, b): the layout whose gradient rows are the sources' grad_output rows
+// gathered in source order ([W*B, sum D]).
+//   merged_offsets [T*W*B+1], merged_indices and merged_scales [sum of lookups].
+int oracle_merge(int32_t T, int32_t B, int32_t W, const int64_t* recv_offsets,
+                 const int64_t* recv_indices, const float* recv_scales,
+                 int64_t* merged_offsets, int64_t* merged_indices, float* merged_scales) {
+  if (T <= 0 || B <= 0 || W <= 0) return ERR_INVALID_ARG;
+  const int64_t BT = static_cast<int64_t>(T) * B;
+  std::vector<int64_t> first(static_cast<size_t>(W) + 1, 0);  // first lookup of each source
+  for (int32_t s = 0; s < W; ++s) {
+    const int64_t* off = recv_offsets + static_cast<int64_t>(s) * (BT + 1);
+    if (off[0] != 0) return ERR_INVALID_ARG;
+    for (int64_t bt = 0; bt < BT; ++bt)
+      if (off[bt + 1] < off[bt]) return ERR_INVALID_ARG;
+    first[s + 1] = first[s] + off[BT];
+  }
+  int64_t pos = 0;
+  merged_offsets[0] = 0;
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t s = 0; s < W; ++s)
+      for (int32_t b = 0; b < B; ++b) {
+        const int64_t* off = recv_offsets + static_cast<int64_t>(s) * (BT + 1);
+        const int64_t bt = static_cast<int64_t>(t) * B + b;
+        for (int64_t i = off[bt]; i < off[bt + 1]; ++i, ++pos) {
+          merged_indices[pos] = recv_indices[first[s] + i];
+          merged_scales[pos] = recv_scales[first[s] + i];
+        }
+        merged_offsets[(static_cast<int64_t>(t) * W + s) * B + b + 1] = pos;
+      }
   return OK;
 }
 
