@@ -56,8 +56,10 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true", help="plain launches instead of programmatic dependent launches")
     ap.add_argument("--path", default="auto", choices=["auto", "sorted", "atomic"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", default="bwd", choices=["bwd", "fwd"],
-                    help="bwd: backward + update (the headline); fwd: forward pooled lookup")
+    ap.add_argument("--op", default="bwd", choices=["bwd", "fwd", "shard"],
+                    help="bwd: backward + update (the headline); fwd: forward pooled lookup; "
+                         "shard: row-sharded step of one rank (W ranks emulated on one GPU)")
+    ap.add_argument("--shards", type=int, default=8, help="ranks W of --op shard")
     return ap.parse_args()
 
 
@@ -324,12 +326,137 @@ def run_forward(args):
     }, default=float))
 
 
+def timed(fn, K, flush, stream):
+    """Mean device ms of fn over K runs (CUDA events on the launching stream, L2
+    flushed before each run)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        starts[k].record(stream)
+        fn()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / K
+
+
+def run_shard(args):
+    """One rank's row-sharded step, W ranks emulated on one GPU: every rank's batch
+    is bucketed by row owner, the all-to-all is replaced by device copies (on a
+    deployment NCCL moves these bytes), and the most loaded owner merges what it
+    receives and runs its backward (B' = W*B). Timed per stage, excluding the
+    exchange itself: bucketize (rank 0's batch; it synchronises for the sizes),
+    merge and backward (the most loaded owner)."""
+    import torch
+    import oracle
+    from sparse_embedding_bag_gb300 import build as b
+    from sparse_embedding_bag_gb300 import embbwd as E
+    from sparse_embedding_bag_gb300 import shard as S
+    from sparse_embedding_bag_gb300 import synth
+    if args.workload not in ("dlrm", "tiny"):
+        raise SystemExit("--op shard needs a workload whose tables do not depend on the seed (dlrm, tiny)")
+    torch.cuda.set_device(0)
+    b.build()
+    E.load()
+    W, K = args.shards, max(args.steps // 10, 20)
+    srcs = [make_workload(args.workload, s, "cpu") for s in range(W)]
+    w = srcs[0]
+    T, B = w.T, w.B
+    rb = S.even_row_bounds(w.rows, W)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda:0")
+    dev_in = [(torch.from_numpy(x.indices).cuda(), torch.from_numpy(x.offsets).cuda()) for x in srcs]
+    maxN = max(x.N for x in srcs)
+    sh = E.emb_shard_create(0, T, W, rb, B)
+    sends = []
+    for (idx, off), x in zip(dev_in, srcs):
+        so = torch.empty((W, T * B + 1), dtype=torch.int64, device="cuda:0")
+        si = torch.empty(maxN, dtype=torch.int64, device="cuda:0")
+        cnt = E.emb_shard_bucketize(sh, idx, off, x.N, B, None, E.EMB_POOL_SUM, so, si, None)
+        sends.append((so, si, cnt))
+    recv_counts = np.sum([c for _, _, c in sends], axis=0)
+    r = int(np.argmax(recv_counts))  # the most loaded owner
+    ro = torch.stack([so[r] for so, _, _ in sends]).contiguous()
+    ri = torch.cat([si[int(c[:r].sum()):int(c[:r].sum()) + int(c[r])] for _, si, c in sends])
+    n = int(ri.numel())
+    mo = torch.empty(T * W * B + 1, dtype=torch.int64, device="cuda:0")
+    mi = torch.empty(max(n, 1), dtype=torch.int64, device="cuda:0")
+    local, hsc, Do, wo = S.local_tables(w.rows, w.dims, rb, r)
+    plan = E.emb_bwd_plan(0, T, hsc, Do, wo, None, w.weight_dtype, w.grad_dtype, max(n, 1), W * B, 0, 0)
+    lo = rb[:, r]
+    wl = torch.from_numpy(np.concatenate([w.weights[w.weights_offsets[t] + lo[t] * w.dims[t]:
+                                                    w.weights_offsets[t] + rb[t, r + 1] * w.dims[t]]
+                                          for t in range(T)])).cuda()
+    ml = torch.full((int(hsc[-1]),), 0.0, dtype=torch.float32, device="cuda:0")
+    grad = torch.from_numpy(np.concatenate([x.grad_output for x in srcs])).cuda()
+    so0, si0 = torch.empty_like(sends[0][0]), torch.empty_like(sends[0][1])
+
+    def bucketize():
+        E.emb_shard_bucketize(sh, dev_in[0][0], dev_in[0][1], srcs[0].N, B, None, E.EMB_POOL_SUM,
+                              so0, si0, None)
+
+    def merge():
+        E.emb_shard_merge(sh, ro, ri, None, n, B, mo, mi, None)
+
+    def backward():
+        if w.optimizer == synth.SGD:
+            E.emb_bag_bwd_sgd(plan, wl, mi, mo, n, W * B, None, grad, E.EMB_POOL_SUM, w.lr)
+        else:
+            E.emb_bag_bwd_rowwise_adagrad(plan, wl, ml, mi, mo, n, W * B, None, grad,
+                                          E.EMB_POOL_SUM, w.lr, w.eps)
+
+    for _ in range(max(args.warmup, 3)):
+        bucketize(); merge(); backward()
+    torch.cuda.synchronize()
+    if E.emb_shard_status(sh) != E.EMB_OK or E.emb_plan_status(plan) != E.EMB_OK:
+        raise SystemExit("device status error")
+    # parity of this configuration's exchange (bit for bit) on the way
+    eo, ei, _, ec = oracle.bucketize(T, B, rb, srcs[0].indices, srcs[0].offsets)
+    assert np.array_equal(so0.cpu().numpy(), eo) and np.array_equal(si0[:srcs[0].N].cpu().numpy(), ei)
+    with ClockSampler(0) as clocks:
+        ms_b = timed(bucketize, K, flush, stream)
+        ms_m = timed(merge, K, flush, stream)
+        ms_r = timed(backward, K, flush, stream)
+    N0, BT = srcs[0].N, T * B
+    bytes_b = 16 * N0 + 8 * (BT + 1) + 8 * W * (BT + 1)       # indices in/out, offsets, per-owner offsets
+    bytes_m = 8 * W * (BT + 1) + 16 * n + 8 * (T * W * B + 1)  # received offsets, indices in/out, merged offsets
+    peak, peak_kind = peaks()
+    stages = {"bucketize": (ms_b, bytes_b), "merge": (ms_m, bytes_m)}
+    dom = max(stages, key=lambda k: stages[k][0])
+    ach = stages[dom][1] / (stages[dom][0] * 1e-3) / 1e9
+    ms = ms_b + ms_m + ms_r
+    print(json.dumps({
+        "metric": "row-sharded embedding step of one rank (exchange kernels + backward): lookups/sec",
+        "op": "shard", "value": n / (ms * 1e-3), "unit": "lookups/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload] + " per rank", "ranks_emulated": W,
+                   "row_split": "even contiguous ranges of every table",
+                   "owner": r, "lookups_received": n, "lookups_per_owner": recv_counts.tolist(),
+                   "excluded": "the all-to-all and all-gather themselves (device copies here)",
+                   "l2": "256 MB buffer written before each timed call"},
+        "stage_ms": {"bucketize": ms_b, "merge": ms_m, "backward_owner": ms_r},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak, "traffic": None},
+        "cpu_baseline": None,
+        # bucketize: count, three scan phases, scatter; merge: bases, copy; backward:
+        # histogram, radix passes, run-length, reduce
+        "gpu_launches": K * (5 + 2 + 3 + -(-max(int(hsc[-1] - 1).bit_length(), 1) // 8)),
+        "clocks": clocks.summary(),
+    }, default=float))
+    E.emb_plan_destroy(plan)
+    E.emb_shard_destroy(sh)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "fwd":
         return run_forward(args)
+    if args.op == "shard":
+        return run_shard(args)
     import torch
     import torch.distributed as dist
 

@@ -266,6 +266,67 @@ emb_status emb_plan_set_profiling(emb_plan* plan, int enable);
  * [0] index check, [4] atomic scatter, others 0. Writes min(n, 5) values. */
 emb_status emb_plan_stage_ms(emb_plan* plan, float* ms, int32_t n);
 
+/* ---- Row-wise sharding over W ranks (the exchange step before the backward).
+ * Every rank trains on its own batch and owns a contiguous row range of every
+ * table: rank r holds rows [row_bounds[t*(W+1)+r], row_bounds[t*(W+1)+r+1]) of
+ * table t, the vocabulary sharding of "Function _embedding_bwd_kernel" (tinygrad:
+ * a device owns one slice of the rows; lookups outside it add nothing there).
+ * A step on rank r:
+ *   1. emb_shard_bucketize its batch: per owner, the lookups of its rows;
+ *   2. all-to-all the parts (offsets: W*(T*B+1) each way; indices and scales
+ *      with the per-owner counts as split sizes) and all-gather grad_output into
+ *      [W*B, sum D] in rank order (e.g. NCCL through torch.distributed);
+ *   3. emb_shard_merge the received parts into one batch of W*B bags per table;
+ *   4. the ordinary backward on the rank's own plan (its local tables: row range
+ *      sizes as hash_size_cumsum, rows relative to the range) with B' = W*B, the
+ *      merged offsets and indices, the merged scales as per_sample_weights (or
+ *      NULL when the batch is unweighted and sum-pooled) and EMB_POOL_SUM.
+ * The forward runs 1-3 the same way, then emb_bag_fwd with B' = W*B gives the
+ * rank's partial sums of every rank's bags, and a reduce-scatter over ranks
+ * gives each rank its own bags' output. */
+typedef struct emb_shard emb_shard;
+
+/* Creates the shard map of one rank: T tables (1..4096), W ranks (1..256),
+ * row_bounds host int64[T*(W+1)] (row_bounds[t*(W+1)] = 0, non-decreasing, last
+ * = rows of table t > 0; empty ranges are allowed here, but a rank whose plan
+ * has an empty table cannot create that plan), max_B the largest per-rank batch
+ * (W * T * max_B < 2^31). Allocates its scratch on `device` (about
+ * 12 * W * T * max_B bytes). */
+emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
+                            const int64_t* row_bounds, int32_t max_B);
+emb_status emb_shard_destroy(emb_shard* shard);
+
+/* Step 1 on `stream`; synchronises it (the exchange needs the sizes on the
+ * host). Inputs as for emb_bag_bwd_sgd (device indices [N], offsets [T*B+1],
+ * optional per_sample_weights [N], mode). Outputs (device, caller-owned):
+ *   send_offsets int64[W][T*B+1]: owner r's bag offsets counted from its first lookup;
+ *   send_indices int64[N]: owner 0's lookups first, then owner 1's, ..., each row
+ *     relative to the owner's range, in bag order and lookup order within a bag;
+ *   send_scales float[N] or NULL: per-sample weight (1 if none), divided in fp32
+ *     by the length of its whole bag under mean pooling;
+ *   send_counts host int64[W]: lookups per owner (the all-to-all split sizes).
+ * EMB_ERR_INDEX_OUT_OF_RANGE for an index outside its table, EMB_ERR_INVALID_ARG
+ * for malformed offsets; nothing usable is written then. */
+emb_status emb_shard_bucketize(emb_shard* shard, const int64_t* indices, const int64_t* offsets,
+                               int64_t N, int32_t B, const float* per_sample_weights,
+                               emb_pooling mode, int64_t* send_offsets, int64_t* send_indices,
+                               float* send_scales, int64_t* send_counts, void* stream);
+
+/* Step 3 on `stream`, asynchronous. recv_offsets device int64[W][T*B+1] (source
+ * s's send_offsets for this rank, in source order), recv_indices / recv_scales
+ * the n_recv received lookups concatenated in source order (recv_scales may be
+ * NULL, then merged_scales must be NULL too). Writes merged_offsets int64[T*W*B+1]
+ * and merged_indices / merged_scales [n_recv]: bag s*B + b of table t holds
+ * source s's bag (t, b). Received offsets inconsistent with n_recv are skipped
+ * and reported by emb_shard_status as EMB_ERR_INVALID_ARG. */
+emb_status emb_shard_merge(emb_shard* shard, const int64_t* recv_offsets, const int64_t* recv_indices,
+                           const float* recv_scales, int64_t n_recv, int32_t B,
+                           int64_t* merged_offsets, int64_t* merged_indices, float* merged_scales,
+                           void* stream);
+
+/* Waits for the shard's last call and returns (and clears) its latched errors. */
+emb_status emb_shard_status(emb_shard* shard);
+
 /* Static description of a status code. */
 const char* emb_status_string(emb_status status);
 

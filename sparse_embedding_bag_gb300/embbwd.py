@@ -31,7 +31,9 @@ EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_r
            "emb_nobag_bwd_sgd", "emb_plan_status", "emb_plan_debug_runs", "emb_plan_set_profiling",
            "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc",
            "emb_bag_fwd", "emb_bag_bwd_adagrad", "emb_bag_bwd_dense_grad",
-           "emb_nobag_bwd_dense_grad", "emb_plan_set_rounding", "emb_plan_get_rounding")
+           "emb_nobag_bwd_dense_grad", "emb_plan_set_rounding", "emb_plan_get_rounding",
+           "emb_shard_create", "emb_shard_destroy", "emb_shard_bucketize", "emb_shard_merge",
+           "emb_shard_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +75,11 @@ def load(path: str = LIB_PATH):
             "emb_nobag_bwd_dense_grad": [vp, vp, vp, vp, i64, i32, vp, vp],
             "emb_plan_set_rounding": [vp, ctypes.c_uint64, ctypes.c_uint64],
             "emb_plan_get_rounding": [vp, vp, vp],
+            "emb_shard_create": [ctypes.POINTER(vp), c_int, i32, i32, vp, i32],
+            "emb_shard_destroy": [vp],
+            "emb_shard_bucketize": [vp, vp, vp, i64, i32, vp, c_int, vp, vp, vp, vp, vp],
+            "emb_shard_merge": [vp, vp, vp, vp, i64, i32, vp, vp, vp, vp],
+            "emb_shard_status": [vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -251,3 +258,45 @@ def emb_nobag_bwd_sgd_atomic_noalloc(device, T, hash_size_cumsum, weights_offset
                                                  _ptr(grad_output), int(grad_dtype), float(lr),
                                                  _ptr(device_status), _stream(stream))
     return _check(st, "emb_nobag_bwd_sgd_atomic_noalloc")
+
+
+# ---- row-wise sharding (exchange step)
+
+def emb_shard_create(device, T, W, row_bounds, max_B):
+    """Shard map of one rank; row_bounds host int64 [T, W+1]. Returns a handle (int)."""
+    rb = _host(row_bounds, np.int64)
+    assert rb.size == T * (W + 1)
+    out = ctypes.c_void_p()
+    _check(load().emb_shard_create(ctypes.byref(out), int(device), int(T), int(W), rb.ctypes.data,
+                                   int(max_B)), "emb_shard_create")
+    return out.value
+
+
+def emb_shard_destroy(shard):
+    return _check(load().emb_shard_destroy(shard), "emb_shard_destroy")
+
+
+def emb_shard_bucketize(shard, indices, offsets, N, B, per_sample_weights, mode, send_offsets,
+                        send_indices, send_scales, stream=None):
+    """Splits the batch by row owner into the send buffers (send_offsets a device
+    int64 tensor [W, T*B+1]); returns the per-owner lookup counts (host int64 [W]).
+    Synchronises the stream."""
+    counts = np.zeros(int(send_offsets.shape[0]), np.int64)
+    st = load().emb_shard_bucketize(shard, _ptr(indices), _ptr(offsets), int(N), int(B),
+                                    _ptr(per_sample_weights), int(mode), _ptr(send_offsets),
+                                    _ptr(send_indices), _ptr(send_scales), counts.ctypes.data,
+                                    _stream(stream))
+    _check(st, "emb_shard_bucketize")
+    return counts
+
+
+def emb_shard_merge(shard, recv_offsets, recv_indices, recv_scales, n_recv, B, merged_offsets,
+                    merged_indices, merged_scales, stream=None):
+    st = load().emb_shard_merge(shard, _ptr(recv_offsets), _ptr(recv_indices), _ptr(recv_scales),
+                                int(n_recv), int(B), _ptr(merged_offsets), _ptr(merged_indices),
+                                _ptr(merged_scales), _stream(stream))
+    return _check(st, "emb_shard_merge")
+
+
+def emb_shard_status(shard):
+    return load().emb_shard_status(shard)
