@@ -86,8 +86,8 @@ def _load():
                                            i32, vp]
             lib.oracle_dense_grad.argtypes = [i32, i32, vp, vp, vp, i64, i32, vp, vp, vp, i64, vp,
                                               i32, i32, i32, vp]
-            lib.oracle_bucketize.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp,
-                                             vp]
+            lib.oracle_bucketize.argtypes = [i32, i32, i32, vp, i32, vp, vp, i64, vp, i32, vp, vp,
+                                             vp, vp]
             lib.oracle_merge.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp]
             for name in ("oracle_sorted_pairs", "oracle_runs", "oracle_row_grads",
                          "oracle_apply_row", "oracle_backward", "oracle_forward",
@@ -257,8 +257,11 @@ def forward(T, B, hash_size_cumsum, D_offsets, weights_offsets, weights, indices
     return out
 
 
-def bucketize(T, B, row_bounds, indices, offsets, *, per_sample_weights=None, mean=False):
-    """A rank's batch split by the owner of each lookup's row (row_bounds [T, W+1]).
+def bucketize(T, B, row_bounds, indices, offsets, *, per_sample_weights=None, mean=False,
+              cyclic=False):
+    """A rank's batch split by the owner of each lookup's row (row_bounds [T, W+1];
+    with cyclic, rank r owns rows r, r + W, ... and only row_bounds[:, W], the
+    rows of every table, is read).
 
     Returns (send_offsets [W, T*B+1], send_indices, send_scales, send_counts [W]):
     owner r's lookups are send_indices[sum(send_counts[:r]) : ...], rows relative
@@ -271,7 +274,7 @@ def bucketize(T, B, row_bounds, indices, offsets, *, per_sample_weights=None, me
     si = np.zeros(idx.size, np.int64)
     ss = np.zeros(idx.size, np.float32)
     sc = np.zeros(W, np.int64)
-    _check(_load().oracle_bucketize(T, B, W, _p(rb), _p(idx), _p(off), idx.size, _p(psw),
+    _check(_load().oracle_bucketize(T, B, W, _p(rb), int(bool(cyclic)), _p(idx), _p(off), idx.size, _p(psw),
                                     int(bool(mean)), _p(so), _p(si), _p(ss), _p(sc)))
     return so, si, ss, sc
 

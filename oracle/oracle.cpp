@@ -553,6 +553,10 @@ int oracle_forward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_of
 // (an all-gather); each owner then runs the backward on the lookups it received,
 // the batches of all ranks side by side, and updates its rows only.
 
+// Cyclic map (cyclic != 0): rank r owns the rows congruent to r modulo W of every
+// table instead, local row = row / W (only row_bounds[t*(W+1) + W], the rows of
+// table t, is read); a skewed id distribution then spreads over all ranks.
+//
 // The bucketing a rank does before the exchange: its batch (T tables x B bags,
 // CSR offsets, table-major) split by owner. Owner r's part lists, bag by bag
 // and in lookup order, the row relative to r's range and the lookup's scale:
@@ -562,7 +566,7 @@ int oracle_forward(int32_t T, int32_t B, const int64_t* hsc, const int32_t* D_of
 //   send_offsets [W][T*B+1]: owner r's bag offsets, counted from its first lookup;
 //   send_indices, send_scales [N]: owner 0's lookups first, then owner 1's, ...;
 //   send_counts [W]: lookups per owner.
-int oracle_bucketize(int32_t T, int32_t B, int32_t W, const int64_t* row_bounds,
+int oracle_bucketize(int32_t T, int32_t B, int32_t W, const int64_t* row_bounds, int32_t cyclic,
                      const int64_t* indices, const int64_t* offsets, int64_t N,
                      const float* per_sample_weights, int32_t mean_pooling,
                      int64_t* send_offsets, int64_t* send_indices, float* send_scales,
@@ -571,6 +575,10 @@ int oracle_bucketize(int32_t T, int32_t B, int32_t W, const int64_t* row_bounds,
   const int64_t BT = static_cast<int64_t>(T) * B;
   for (int32_t t = 0; t < T; ++t) {
     const int64_t* rb = row_bounds + static_cast<int64_t>(t) * (W + 1);
+    if (cyclic) {
+      if (rb[W] <= 0) return ERR_INVALID_ARG;
+      continue;
+    }
     if (rb[0] != 0) return ERR_INVALID_ARG;
     for (int32_t r = 0; r < W; ++r)
       if (rb[r + 1] < rb[r]) return ERR_INVALID_ARG;
@@ -589,12 +597,19 @@ int oracle_bucketize(int32_t T, int32_t B, int32_t W, const int64_t* row_bounds,
       const int64_t row = indices[i];
       if (row < 0 || row >= rb[W]) return ERR_INDEX_OUT_OF_RANGE;
       int32_t r = 0;
-      while (!(row >= rb[r] && row < rb[r + 1])) ++r;  // empty ranges never match
+      int64_t local = 0;
+      if (cyclic) {
+        r = static_cast<int32_t>(row % W);
+        local = row / W;
+      } else {
+        while (!(row >= rb[r] && row < rb[r + 1])) ++r;  // empty ranges never match
+        local = row - rb[r];
+      }
       float s = per_sample_weights ? per_sample_weights[i] : 1.0f;
       // fp32 quotient, rounded once: the double quotient of two floats rounds to
       // the same fp32 value (53 >= 2 * 24 + 2 bits)
       if (mean_pooling) s = static_cast<float>(static_cast<double>(s) / static_cast<double>(static_cast<float>(L)));
-      idx[r].push_back(row - rb[r]);
+      idx[r].push_back(local);
       scale[r].push_back(s);
     }
     for (int32_t r = 0; r < W; ++r)

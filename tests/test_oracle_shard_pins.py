@@ -70,6 +70,31 @@ def test_brute_force_uneven_ranges(oracle_mod):
             assert all(0 <= i < rb[t, r + 1] - rb[t, r] for i, _ in got)
 
 
+def cyclic_bounds(rows, W):
+    """The row counts in the last column (all a cyclic map reads)."""
+    rb = np.zeros((len(rows), W + 1), np.int64)
+    rb[:, W] = rows
+    return rb
+
+
+@pytest.mark.parametrize("W", [1, 4])
+def test_cyclic_brute_force(oracle_mod, W):
+    rows = [60, 3, 33]  # table 1 has fewer rows than ranks: rank 3 owns none of it
+    w = batch(4, rows, [4, 4, 8], 15, max_len=9, weighted=True)
+    so, si, ss, sc = oracle_mod.bucketize(w.T, w.B, cyclic_bounds(rows, W), w.indices, w.offsets,
+                                          per_sample_weights=w.per_sample_weights, cyclic=True)
+    assert sc.sum() == w.N
+    start = np.concatenate([[0], np.cumsum(sc)])
+    for r in range(W):
+        for bt in range(w.T * w.B):
+            want = [(int(w.indices[i]) // W, w.per_sample_weights[i])
+                    for i in range(w.offsets[bt], w.offsets[bt + 1]) if int(w.indices[i]) % W == r]
+            a, b = start[r] + so[r, bt], start[r] + so[r, bt + 1]
+            assert list(zip(si[a:b].tolist(), ss[a:b].tolist())) == [(i, float(s)) for i, s in want]
+    if W == 1:
+        assert np.array_equal(si, w.indices) and np.array_equal(so[0], w.offsets)
+
+
 def test_out_of_range_index_is_an_error(oracle_mod):
     w = batch(3, [10, 10], [4, 4], 4, max_len=3)
     w.indices[-1] = 10
@@ -77,10 +102,10 @@ def test_out_of_range_index_is_an_error(oracle_mod):
         oracle_mod.bucketize(w.T, w.B, even_bounds(w.rows, 2), w.indices, w.offsets)
 
 
-def exchange(oracle_mod, sources, rb, mean):
+def exchange(oracle_mod, sources, rb, mean, cyclic=False):
     """Bucketize every source's batch and deliver owner r's parts, in source order."""
     parts = [oracle_mod.bucketize(src.T, src.B, rb, src.indices, src.offsets,
-                                  per_sample_weights=src.per_sample_weights, mean=mean)
+                                  per_sample_weights=src.per_sample_weights, mean=mean, cyclic=cyclic)
              for src in sources]
     W = rb.shape[1] - 1
     recv = []
@@ -133,57 +158,70 @@ def test_merge_equals_global_batch_by_brute_force(oracle_mod):
         assert np.all(ms == 1.0)
 
 
-def shard_layout(w, rb, r):
-    """Owner r's tables: its row range of every table (hash_size_cumsum, weights
-    offsets, weights and row-wise state sliced from the full arrays)."""
-    lo, hi = rb[:, r], rb[:, r + 1]
-    local = (hi - lo).astype(np.int64)
+def owned_rows(w, rb, r, cyclic):
+    """Rows of every table that owner r holds, in its local order."""
+    W = rb.shape[1] - 1
+    if cyclic:
+        return [np.arange(r, int(w.rows[t]), W) for t in range(w.T)]
+    return [np.arange(rb[t, r], rb[t, r + 1]) for t in range(w.T)]
+
+
+def shard_layout(w, rb, r, cyclic=False):
+    """Owner r's tables: its rows of every table (hash_size_cumsum, weights
+    offsets, weights and row-wise state gathered from the full arrays)."""
+    own = owned_rows(w, rb, r, cyclic)
+    local = np.array([o.size for o in own], np.int64)
     hsc = np.concatenate([[0], np.cumsum(local)]).astype(np.int64)
     wo = np.concatenate([[0], np.cumsum(local * w.dims)[:-1]]).astype(np.int64)
-    weights = np.concatenate([w.weights[w.weights_offsets[t] + lo[t] * w.dims[t]:
-                                        w.weights_offsets[t] + hi[t] * w.dims[t]] for t in range(w.T)])
+    weights = np.concatenate([w.weights[(w.weights_offsets[t] + own[t][:, None] * w.dims[t] +
+                                         np.arange(w.dims[t])).reshape(-1)] for t in range(w.T)])
     mom = None if w.momentum is None else np.concatenate(
-        [w.momentum[w.hash_size_cumsum[t] + lo[t]:w.hash_size_cumsum[t] + hi[t]] for t in range(w.T)])
+        [w.momentum[w.hash_size_cumsum[t] + own[t]] for t in range(w.T)])
     return hsc, wo, weights.copy(), mom
 
 
-def unshard(w, rb, shards):
-    """Full weights (and state) from the owners' slices."""
+def unshard(w, rb, shards, cyclic=False):
+    """Full weights (and state) from the owners' rows."""
     weights, mom = np.array(w.weights, copy=True), None if w.momentum is None else w.momentum.copy()
     for r, (sw, sm) in enumerate(shards):
-        hsc, wo, _, _ = shard_layout(w, rb, r)
+        hsc, wo, _, _ = shard_layout(w, rb, r, cyclic)
+        own = owned_rows(w, rb, r, cyclic)
         for t in range(w.T):
-            lo, hi, D = rb[t, r], rb[t, r + 1], int(w.dims[t])
-            weights[w.weights_offsets[t] + lo * D:w.weights_offsets[t] + hi * D] = \
-                sw[wo[t]:wo[t] + (hi - lo) * D]
+            D = int(w.dims[t])
+            dst = (w.weights_offsets[t] + own[t][:, None] * D + np.arange(D)).reshape(-1)
+            weights[dst] = sw[wo[t]:wo[t] + own[t].size * D]
             if mom is not None:
-                mom[w.hash_size_cumsum[t] + lo:w.hash_size_cumsum[t] + hi] = sm[hsc[t]:hsc[t + 1]]
+                mom[w.hash_size_cumsum[t] + own[t]] = sm[hsc[t]:hsc[t + 1]]
     return weights, mom
 
 
-@pytest.mark.parametrize("opt,weighted,mean", [(synth.SGD, False, False), (synth.SGD, True, True),
-                                               (synth.ROWWISE_ADAGRAD, False, False),
-                                               (synth.ROWWISE_ADAGRAD, True, False),
-                                               (synth.SGD, False, True)])
-def test_sharded_step_equals_unsharded(oracle_mod, opt, weighted, mean):
+@pytest.mark.parametrize("opt,weighted,mean,cyclic", [(synth.SGD, False, False, False),
+                                                      (synth.SGD, True, True, False),
+                                                      (synth.ROWWISE_ADAGRAD, False, False, False),
+                                                      (synth.ROWWISE_ADAGRAD, True, False, False),
+                                                      (synth.SGD, False, True, False),
+                                                      (synth.SGD, False, False, True),
+                                                      (synth.ROWWISE_ADAGRAD, True, True, True)])
+def test_sharded_step_equals_unsharded(oracle_mod, opt, weighted, mean, cyclic):
     rows, dims, B, W = [70, 25, 300], [8, 4, 16], 12, 3
     sources = [batch(20 + s, rows, dims, B, max_len=8, weighted=weighted, optimizer=opt)
                for s in range(W)]
     w = sources[0]  # the model (weights, state) is the same on every source
-    rb = even_bounds(rows, W)
-    rb[1] = [0, 3, 4, 25]  # uneven: an owner with one row of table 1
-    recv = exchange(oracle_mod, sources, rb, mean)
+    rb = cyclic_bounds(rows, W) if cyclic else even_bounds(rows, W)
+    if not cyclic:
+        rb[1] = [0, 3, 4, 25]  # uneven: an owner with one row of table 1
+    recv = exchange(oracle_mod, sources, rb, mean, cyclic)
     gidx, goff, gpsw, grad, GB = global_batch(sources)
     shards = []
     for r in range(W):
         mo, mi, ms = oracle_mod.merge(w.T, B, W, *recv[r])
-        hsc, wo, weights, mom = shard_layout(w, rb, r)
+        hsc, wo, weights, mom = shard_layout(w, rb, r, cyclic)
         if mi.size:
             oracle_mod.backward(w.T, GB, hsc, w.D_offsets, wo, weights, mi, mo, grad,
                                 optimizer=opt, lr=w.lr, eps=w.eps, momentum=mom,
                                 per_sample_weights=None if not (weighted or mean) else ms)
         shards.append((weights, mom))
-    got_w, got_m = unshard(w, rb, shards)
+    got_w, got_m = unshard(w, rb, shards, cyclic)
     ref_w = np.array(w.weights, copy=True)
     ref_m = None if w.momentum is None else w.momentum.copy()
     oracle_mod.backward(w.T, GB, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, ref_w, gidx,
