@@ -294,6 +294,13 @@ typedef struct emb_shard emb_shard;
  * 12 * W * T * max_B bytes). */
 emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
                             const int64_t* row_bounds, int32_t max_B);
+
+/* The cyclic map: rank r owns rows r, r + W, r + 2W, ... of every table (its
+ * local row k is row k*W + r), so a skewed id distribution spreads over all
+ * ranks. rows: host int64[T], each > 0. Rows are then relative as row / W in
+ * send_indices; a rank's plan has ceil((rows_t - r) / W) rows of table t. */
+emb_status emb_shard_create_cyclic(emb_shard** out, int device, int32_t T, int32_t W,
+                                   const int64_t* rows, int32_t max_B);
 emb_status emb_shard_destroy(emb_shard* shard);
 
 /* Step 1 on `stream`; synchronises it (the exchange needs the sizes on the
@@ -301,7 +308,8 @@ emb_status emb_shard_destroy(emb_shard* shard);
  * optional per_sample_weights [N], mode). Outputs (device, caller-owned):
  *   send_offsets int64[W][T*B+1]: owner r's bag offsets counted from its first lookup;
  *   send_indices int64[N]: owner 0's lookups first, then owner 1's, ..., each row
- *     relative to the owner's range, in bag order and lookup order within a bag;
+ *     relative to the owner's range (cyclic map: row / W), in bag order and
+ *     lookup order within a bag;
  *   send_scales float[N] or NULL: per-sample weight (1 if none), divided in fp32
  *     by the length of its whole bag under mean pooling;
  *   send_counts host int64[W]: lookups per owner (the all-to-all split sizes).

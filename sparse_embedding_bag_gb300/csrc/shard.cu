@@ -1,7 +1,9 @@
 // Row-wise sharding over W ranks: the exchange step of a deployment in which
 // every rank trains on its own batch and owns a contiguous row range of every
 // table (the vocabulary sharding of "Function _embedding_bwd_kernel": a device
-// owns one slice of the rows and lookups outside it add nothing there).
+// owns one slice of the rows and lookups outside it add nothing there), or, in
+// the cyclic map, the rows congruent to its rank modulo W (local row = row / W),
+// which spreads a skewed id distribution over all ranks.
 //
 //   bucketize (on every source rank): each lookup of the rank's batch goes to the
 //     owner of its row; per owner, bag by bag in lookup order, the row relative to
@@ -33,10 +35,11 @@ struct BucketArgs {
   const int64_t* indices;
   const int64_t* offsets;   // [T*B+1]
   const float* psw;         // nullable
-  const int64_t* bounds;    // [T][W+1]
+  const int64_t* bounds;    // [T][W+1] (cyclic: only [t][W], the rows of table t)
   int64_t N;
   uint32_t T, B, W;
   int mean;
+  int cyclic;
   uint32_t* cnt;            // [W][T*B]: lookups of bag bt owned by r
   const int64_t* pos;       // [W*T*B+1]: exclusive scan of cnt
   int64_t* send_offsets;    // [W][T*B+1]
@@ -82,6 +85,19 @@ __device__ __forceinline__ uint32_t owner_of(const int64_t* rb, uint32_t W, int6
     else hi = mid;
   }
   return lo;
+}
+
+// Owner of `row` (0 <= row < rows of its table) and the row's index on it.
+__device__ __forceinline__ uint32_t route_row(const BucketArgs& a, const int64_t* rb, int64_t row,
+                                              int64_t* local) {
+  if (a.cyclic) {
+    const int64_t q = row / a.W;
+    *local = q;
+    return (uint32_t)(row - q * a.W);
+  }
+  const uint32_t r = owner_of(rb, a.W, row);
+  *local = row - __ldg(&rb[r]);
+  return r;
 }
 
 // Exclusive scan of one int64 per thread over the block; *total gets the sum.
@@ -140,7 +156,8 @@ __global__ void __launch_bounds__(kThreads) k_bucket_count(BucketArgs a) {
         bad_index = true;
         continue;
       }
-      atomicAdd(&s_cnt[warp][owner_of(rb, a.W, row)], 1u);
+      int64_t local;
+      atomicAdd(&s_cnt[warp][route_row(a, rb, row, &local)], 1u);
     }
     __syncwarp();
     for (uint32_t r = lane; r < a.W; r += 32) {
@@ -230,10 +247,10 @@ __global__ void __launch_bounds__(kThreads) k_bucket_scatter(BucketArgs a) {
     for (int64_t i0 = s; i0 < e; i0 += 32) {
       const int64_t i = i0 + lane;
       int32_t r = -1;
-      int64_t row = 0;
+      int64_t local = 0;
       if (i < e) {
-        row = a.indices[i];
-        if (row >= 0 && row < rows) r = (int32_t)owner_of(rb, a.W, row);
+        const int64_t row = a.indices[i];
+        if (row >= 0 && row < rows) r = (int32_t)route_row(a, rb, row, &local);
       }
       const uint32_t peers = __match_any_sync(0xffffffffu, r);
       const uint32_t before = __popc(peers & lanemask_lt_());
@@ -242,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) k_bucket_scatter(BucketArgs a) {
         if (p < 0 || p >= a.N) {
           overflow = true;
         } else {
-          a.send_indices[p] = row - __ldg(&rb[r]);
+          a.send_indices[p] = local;
           if (a.send_scales) {
             float sc = a.psw ? a.psw[i] : 1.0f;
             if (a.mean) sc = __fdiv_rn(sc, L);
@@ -307,35 +324,62 @@ __global__ void __launch_bounds__(kThreads) k_merge_bases(MergeArgs a) {
   if (threadIdx.x == 0) a.merged_offsets[(uint64_t)a.T * a.W * a.B] = carry;
 }
 
-// Merge phase 2: one warp per merged bag (t, s, b) copies source s's bag (t, b)
-// and writes its offset. Received offsets are checked against the received
-// lookups; a bag that does not fit is skipped and reported.
+// Merge phase 2. Offsets: merged bag q = (t*W + s)*B + b starts at the first
+// merged lookup of block (t, s) plus bag b's place in source s's table-t part.
+// Lookups: every (t, s) block is contiguous on both sides (source s's table-t
+// lookups, in the received buffer and in the merged one), so each merged
+// position j copies from its block's source start plus its offset in the block,
+// the block found by a search of the block starts (staged in shared memory
+// when they fit): coalesced reads and writes. Received offsets are checked
+// against the received lookups; what does not fit is skipped and reported.
+constexpr uint32_t kMergeStage = 2048;
+
 __global__ void __launch_bounds__(kThreads) k_merge_copy(MergeArgs a) {
-  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ int64_t s_base[kMergeStage];
   const uint64_t BT = (uint64_t)a.T * a.B, WB = (uint64_t)a.W * a.B, Q = (uint64_t)a.T * WB;
-  const int64_t* first = a.bases + (uint64_t)a.T * a.W;
+  const uint64_t TW = (uint64_t)a.T * a.W;
+  const int64_t* first = a.bases + TW;
+  const bool staged = TW <= kMergeStage;
+  if (staged) {
+    for (uint32_t k = threadIdx.x; k < TW; k += kThreads) s_base[k] = a.bases[k];
+    __syncthreads();
+  }
   bool bad = false;
-  for (uint64_t q = (uint64_t)blockIdx.x * kWarps + warp; q < Q; q += (uint64_t)gridDim.x * kWarps) {
+  const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+  for (uint64_t q = (uint64_t)blockIdx.x * kThreads + threadIdx.x; q < Q; q += stride) {
     const uint64_t t = q / WB, rem = q - t * WB, s = rem / a.B, b = rem - s * a.B;
     const int64_t* ro = a.recv_offsets + s * (BT + 1);
     const int64_t t0 = ro[t * a.B], lo = ro[t * a.B + b], hi = ro[t * a.B + b + 1];
-    // every term is checked against n_recv < 2^31 before it is added, so no sum overflows
-    const int64_t f = first[s], base = a.bases[t * a.W + s];
-    bool ok = 0 <= t0 && t0 <= lo && lo <= hi && hi <= a.n_recv && 0 <= f && f <= a.n_recv &&
-              0 <= base && base <= a.n_recv;
-    ok = ok && f + hi <= first[s + 1] && f + hi <= a.n_recv && base + (hi - t0) <= a.n_recv;
-    const int64_t dst = ok ? base + (lo - t0) : 0;
-    if (lane == 0) a.merged_offsets[q] = ok ? dst : 0;
+    const int64_t base = staged ? s_base[t * a.W + s] : a.bases[t * a.W + s];
+    // every term is checked against n_recv < 2^31 before it is added
+    const bool ok = 0 <= t0 && t0 <= lo && lo <= hi && hi <= a.n_recv && 0 <= base &&
+                    base <= a.n_recv && base + (lo - t0) <= a.n_recv;
+    a.merged_offsets[q] = ok ? base + (lo - t0) : 0;
+    bad |= !ok;
+  }
+  const int64_t total = min(first[a.W], a.n_recv);
+  for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < (uint64_t)max(total, (int64_t)0); j += stride) {
+    // the block (t, s): the largest k with base[k] <= j (empty blocks never match)
+    uint32_t lo = 0, hi = (uint32_t)TW;
+    while (hi - lo > 1) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if ((staged ? s_base[mid] : a.bases[mid]) <= (int64_t)j) lo = mid;
+      else hi = mid;
+    }
+    const uint32_t t = lo / a.W, s = lo - t * a.W;
+    const int64_t base = staged ? s_base[lo] : a.bases[lo];
+    const int64_t f = first[s], t0 = a.recv_offsets[(uint64_t)s * (BT + 1) + (uint64_t)t * a.B];
+    const bool ok = 0 <= f && f <= a.n_recv && 0 <= t0 && t0 <= a.n_recv && base <= (int64_t)j &&
+                    f + t0 + ((int64_t)j - base) < a.n_recv;
     if (!ok) {
       bad = true;
       continue;
     }
-    for (int64_t i = lo + lane; i < hi; i += 32) {
-      a.merged_indices[dst + (i - lo)] = a.recv_indices[first[s] + i];
-      if (a.merged_scales) a.merged_scales[dst + (i - lo)] = a.recv_scales[first[s] + i];
-    }
+    const int64_t src = f + t0 + ((int64_t)j - base);
+    a.merged_indices[j] = a.recv_indices[src];
+    if (a.merged_scales) a.merged_scales[j] = a.recv_scales[src];
   }
-  if (bad && lane == 0) atomicOr(a.err, kErrOffsets);
+  if (bad) atomicOr(a.err, kErrOffsets);
 }
 
 int warp_grid(uint64_t items, int sms) {
@@ -375,6 +419,7 @@ using namespace embbwd;
 struct emb_shard {
   int device = 0;
   int32_t T = 0, W = 0, max_B = 0;
+  int cyclic = 0;
   int sms = 1;
   int64_t* d_bounds = nullptr;  // [T][W+1]
   uint32_t* cnt = nullptr;      // [W][T*max_B]
@@ -417,10 +462,11 @@ emb_status take_errors(emb_shard* sh) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
-                            const int64_t* row_bounds, int32_t max_B) {
+// row_bounds: [T][W+1] ranges, or (cyclic) only [t][W] = rows of table t is used.
+emb_status create_shard(emb_shard** out, int device, int32_t T, int32_t W,
+                        const int64_t* row_bounds, int32_t max_B, int cyclic) {
   if (!out) return EMB_ERR_INVALID_ARG;
   *out = nullptr;
   if (T <= 0 || T > kMaxT || W <= 0 || W > kMaxW || max_B <= 0 || !row_bounds) return EMB_ERR_INVALID_ARG;
@@ -428,7 +474,9 @@ emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
   if ((uint64_t)W * BT >= (1ull << 31)) return EMB_ERR_INVALID_ARG;
   for (int32_t t = 0; t < T; ++t) {
     const int64_t* rb = row_bounds + (int64_t)t * (W + 1);
-    if (rb[0] != 0 || rb[W] <= 0) return EMB_ERR_INVALID_ARG;
+    if (rb[W] <= 0) return EMB_ERR_INVALID_ARG;
+    if (cyclic) continue;
+    if (rb[0] != 0) return EMB_ERR_INVALID_ARG;
     for (int32_t r = 0; r < W; ++r)
       if (rb[r + 1] < rb[r]) return EMB_ERR_INVALID_ARG;
   }
@@ -439,6 +487,7 @@ emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
   sh->T = T;
   sh->W = W;
   sh->max_B = max_B;
+  sh->cyclic = cyclic;
   int sms = 1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess) sh->sms = sms;
   const uint64_t n = (uint64_t)W * BT;
@@ -465,6 +514,23 @@ emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
   }
   *out = sh;
   return EMB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+emb_status emb_shard_create(emb_shard** out, int device, int32_t T, int32_t W,
+                            const int64_t* row_bounds, int32_t max_B) {
+  return create_shard(out, device, T, W, row_bounds, max_B, 0);
+}
+
+emb_status emb_shard_create_cyclic(emb_shard** out, int device, int32_t T, int32_t W,
+                                   const int64_t* rows, int32_t max_B) {
+  if (!rows || T <= 0 || T > kMaxT || W <= 0 || W > kMaxW) return EMB_ERR_INVALID_ARG;
+  std::vector<int64_t> rb((size_t)T * (W + 1), 0);
+  for (int32_t t = 0; t < T; ++t) rb[(size_t)t * (W + 1) + W] = rows[t];
+  return create_shard(out, device, T, W, rb.data(), max_B, 1);
 }
 
 emb_status emb_shard_destroy(emb_shard* sh) {
@@ -502,6 +568,7 @@ emb_status emb_shard_bucketize(emb_shard* sh, const int64_t* indices, const int6
   a.B = (uint32_t)B;
   a.W = (uint32_t)sh->W;
   a.mean = mode == EMB_POOL_MEAN;
+  a.cyclic = sh->cyclic;
   a.cnt = sh->cnt;
   a.pos = sh->pos;
   a.send_offsets = send_offsets;
@@ -581,9 +648,11 @@ emb_status emb_shard_merge(emb_shard* sh, const int64_t* recv_offsets, const int
   if (cudaError_t e = launch_kernel(reinterpret_cast<const void*>(&k_merge_bases), dim3(1),
                                     dim3(kThreads), 0, s, args, false))
     return status_of(e);
-  const uint64_t Q = (uint64_t)sh->T * sh->W * (uint64_t)B;
+  const uint64_t items = std::max<uint64_t>((uint64_t)sh->T * sh->W * (uint64_t)B, (uint64_t)n_recv);
+  const uint64_t blocks = std::min<uint64_t>((items + kThreads - 1) / kThreads, (uint64_t)sh->sms * 8);
   if (cudaError_t e = launch_kernel(reinterpret_cast<const void*>(&k_merge_copy),
-                                    dim3(warp_grid(Q, sh->sms)), dim3(kThreads), 0, s, args, false))
+                                    dim3((unsigned)std::max<uint64_t>(blocks, 1)), dim3(kThreads), 0, s,
+                                    args, false))
     return status_of(e);
   return EMB_OK;
 }

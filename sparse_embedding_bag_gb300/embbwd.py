@@ -32,8 +32,8 @@ EXPORTS = ("emb_bwd_plan", "emb_plan_destroy", "emb_bag_bwd_sgd", "emb_bag_bwd_r
            "emb_plan_stage_ms", "emb_status_string", "emb_nobag_bwd_sgd_atomic_noalloc",
            "emb_bag_fwd", "emb_bag_bwd_adagrad", "emb_bag_bwd_dense_grad",
            "emb_nobag_bwd_dense_grad", "emb_plan_set_rounding", "emb_plan_get_rounding",
-           "emb_shard_create", "emb_shard_destroy", "emb_shard_bucketize", "emb_shard_merge",
-           "emb_shard_status")
+           "emb_shard_create", "emb_shard_create_cyclic", "emb_shard_destroy", "emb_shard_bucketize",
+           "emb_shard_merge", "emb_shard_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
             "emb_plan_set_rounding": [vp, ctypes.c_uint64, ctypes.c_uint64],
             "emb_plan_get_rounding": [vp, vp, vp],
             "emb_shard_create": [ctypes.POINTER(vp), c_int, i32, i32, vp, i32],
+            "emb_shard_create_cyclic": [ctypes.POINTER(vp), c_int, i32, i32, vp, i32],
             "emb_shard_destroy": [vp],
             "emb_shard_bucketize": [vp, vp, vp, i64, i32, vp, c_int, vp, vp, vp, vp, vp],
             "emb_shard_merge": [vp, vp, vp, vp, i64, i32, vp, vp, vp, vp],
@@ -269,6 +270,16 @@ def emb_shard_create(device, T, W, row_bounds, max_B):
     out = ctypes.c_void_p()
     _check(load().emb_shard_create(ctypes.byref(out), int(device), int(T), int(W), rb.ctypes.data,
                                    int(max_B)), "emb_shard_create")
+    return out.value
+
+
+def emb_shard_create_cyclic(device, T, W, rows, max_B):
+    """Cyclic shard map (rank r owns rows r, r + W, ...); rows host int64 [T]."""
+    rw = _host(rows, np.int64)
+    assert rw.size == T
+    out = ctypes.c_void_p()
+    _check(load().emb_shard_create_cyclic(ctypes.byref(out), int(device), int(T), int(W),
+                                          rw.ctypes.data, int(max_B)), "emb_shard_create_cyclic")
     return out.value
 
 

@@ -2,7 +2,9 @@
 
 Every rank trains on its own batch and owns a contiguous row range of every
 table, the vocabulary sharding of "Function _embedding_bwd_kernel" (tinygrad:
-a device owns one slice of the rows, lookups outside it add nothing there).
+a device owns one slice of the rows, lookups outside it add nothing there), or
+with cyclic=True the rows congruent to its rank modulo W (row k*W + r is local
+row k of rank r), which spreads a skewed id distribution over all ranks.
 One step on every rank:
 
   route     the library buckets the rank's lookups by row owner
@@ -33,11 +35,22 @@ def even_row_bounds(rows, world):
     return np.array([[int(r) * k // world for k in range(world + 1)] for r in rows], np.int64)
 
 
-def local_tables(rows, dims, row_bounds, rank):
-    """The rank's own tables: (rows, hash_size_cumsum, D_offsets, weights_offsets)
-    of its row range of every table, weights packed table after table."""
+def owned_rows(rows, row_bounds, rank, world, cyclic=False):
+    """Global rows of every table that the rank owns, in its local order."""
+    if cyclic:
+        return [np.arange(rank, int(r), world, dtype=np.int64) for r in rows]
     rb = np.asarray(row_bounds, np.int64)
-    local = (rb[:, rank + 1] - rb[:, rank]).astype(np.int64)
+    return [np.arange(rb[t, rank], rb[t, rank + 1], dtype=np.int64) for t in range(len(rows))]
+
+
+def local_tables(rows, dims, row_bounds, rank, world=None, cyclic=False):
+    """The rank's own tables: (rows, hash_size_cumsum, D_offsets, weights_offsets)
+    of its rows of every table, weights packed table after table."""
+    if cyclic:
+        local = np.array([(int(r) - rank + world - 1) // world for r in rows], np.int64)
+    else:
+        rb = np.asarray(row_bounds, np.int64)
+        local = (rb[:, rank + 1] - rb[:, rank]).astype(np.int64)
     dims = np.asarray(dims, np.int64)
     hsc = np.concatenate([[0], np.cumsum(local)]).astype(np.int64)
     D_offsets = np.concatenate([[0], np.cumsum(dims)]).astype(np.int32)
@@ -48,8 +61,11 @@ def local_tables(rows, dims, row_bounds, rank):
 class CudaOps:
     """The four library steps of one rank (C ABI calls on its device)."""
 
-    def __init__(self, device, T, world, row_bounds, max_B, plan):
-        self.shard = E.emb_shard_create(device, T, world, row_bounds, max_B)
+    def __init__(self, device, T, world, row_bounds, max_B, plan, rows=None, cyclic=False):
+        if cyclic:
+            self.shard = E.emb_shard_create_cyclic(device, T, world, rows, max_B)
+        else:
+            self.shard = E.emb_shard_create(device, T, world, row_bounds, max_B)
         self.plan = plan
 
     def bucketize(self, indices, offsets, N, B, psw, mode, send_offsets, send_indices, send_scales):
@@ -95,29 +111,31 @@ class Routed:
 class RowShardedBags:
     """One rank's part of row-wise sharded embedding bags.
 
-    rows, dims: the full tables; row_bounds [T, W+1] (default: even ranges);
+    rows, dims: the full tables; row_bounds [T, W+1] (default: even ranges), or
+    cyclic=True for the modulo-W map;
     max_B: the largest per-rank batch; max_N: the most lookups one rank sends or
     receives per step. The rank's weights and state are its local tables
     (local_tables()); all ranks pass the same B, pooling and weighting.
     """
 
-    def __init__(self, rows, dims, rank, world, max_B, max_N, *, row_bounds=None, group=None,
-                 device="cuda", weight_dtype=0, grad_dtype=0, flags=0, ops=None):
+    def __init__(self, rows, dims, rank, world, max_B, max_N, *, row_bounds=None, cyclic=False,
+                 group=None, device="cuda", weight_dtype=0, grad_dtype=0, flags=0, ops=None):
         import torch
         self.rows, self.dims = np.asarray(rows, np.int64), np.asarray(dims, np.int64)
         self.T, self.rank, self.world = len(self.rows), rank, world
+        self.cyclic = cyclic
         self.row_bounds = even_row_bounds(rows, world) if row_bounds is None else np.asarray(row_bounds, np.int64)
         self.max_B, self.max_N, self.group = max_B, max_N, group
         self.device = torch.device(device)
         self.local_rows, self.hsc, self.D_offsets, self.weights_offsets = local_tables(
-            self.rows, self.dims, self.row_bounds, rank)
+            self.rows, self.dims, self.row_bounds, rank, world, cyclic)
         self.plan = None
         if ops is None:
             dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
             self.plan = E.emb_bwd_plan(dev_index, self.T, self.hsc, self.D_offsets,
                                        self.weights_offsets, None, weight_dtype, grad_dtype,
                                        max_N, world * max_B, 0, flags)
-            ops = CudaOps(dev_index, self.T, world, self.row_bounds, max_B, self.plan)
+            ops = CudaOps(dev_index, self.T, world, self.row_bounds, max_B, self.plan, self.rows, cyclic)
         self.ops = ops
         BT = self.T * max_B
         i64 = torch.int64

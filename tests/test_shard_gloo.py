@@ -44,15 +44,15 @@ def _batch(rank, weighted, optimizer):
 class OracleOps:
     """The four library steps of one rank, computed by the oracle on CPU tensors."""
 
-    def __init__(self, T, row_bounds, hsc, D_offsets, weights_offsets):
-        self.T, self.rb = T, row_bounds
+    def __init__(self, T, row_bounds, hsc, D_offsets, weights_offsets, cyclic):
+        self.T, self.rb, self.cyclic = T, row_bounds, cyclic
         self.hsc, self.Do, self.wo = hsc, D_offsets, weights_offsets
 
     def bucketize(self, indices, offsets, N, B, psw, mode, send_offsets, send_indices, send_scales):
         import oracle
         so, si, ss, sc = oracle.bucketize(self.T, B, self.rb, indices[:N].numpy(), offsets.numpy(),
                                           per_sample_weights=None if psw is None else psw.numpy(),
-                                          mean=(mode == 1))
+                                          mean=(mode == 1), cyclic=self.cyclic)
         send_offsets.numpy()[:] = so
         send_indices.numpy()[:N] = si
         if send_scales is not None:
@@ -99,20 +99,21 @@ def _worker(rank, world, port, mode, out):
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        weighted, mean = mode in ("weighted", "weighted_mean"), mode in ("mean", "weighted_mean")
-        optimizer = synth.ROWWISE_ADAGRAD if mode == "adagrad" else synth.SGD
+        weighted, mean = "weighted" in mode, "mean" in mode
+        optimizer = synth.ROWWISE_ADAGRAD if "adagrad" in mode else synth.SGD
+        cyclic = "cyclic" in mode
         w, own = _batch(rank, weighted, optimizer)
         rb = S.even_row_bounds(ROWS, world)
-        local, hsc, Do, wo = S.local_tables(ROWS, DIMS, rb, rank)
-        ops = OracleOps(len(ROWS), rb, hsc, Do, wo)
-        sb = S.RowShardedBags(ROWS, DIMS, rank, world, B, 4096, device="cpu", ops=ops)
-        lo, hi = rb[:, rank], rb[:, rank + 1]
+        local, hsc, Do, wo = S.local_tables(ROWS, DIMS, rb, rank, world, cyclic)
+        ops = OracleOps(len(ROWS), rb, hsc, Do, wo, cyclic)
+        sb = S.RowShardedBags(ROWS, DIMS, rank, world, B, 4096, device="cpu", ops=ops, cyclic=cyclic)
+        own_rows = S.owned_rows(ROWS, rb, rank, world, cyclic)
         weights = torch.from_numpy(np.concatenate(
-            [w.weights[w.weights_offsets[t] + lo[t] * DIMS[t]:w.weights_offsets[t] + hi[t] * DIMS[t]]
+            [w.weights[(w.weights_offsets[t] + own_rows[t][:, None] * DIMS[t] + np.arange(DIMS[t])).reshape(-1)]
              for t in range(len(ROWS))]).copy())
         mom = torch.from_numpy(np.concatenate(
-            [w.momentum[w.hash_size_cumsum[t] + lo[t]:w.hash_size_cumsum[t] + hi[t]]
-             for t in range(len(ROWS))]).copy()) if w.momentum is not None else None
+            [w.momentum[w.hash_size_cumsum[t] + own_rows[t]] for t in range(len(ROWS))]).copy()) \
+            if w.momentum is not None else None
         idx, off = torch.from_numpy(own.indices), torch.from_numpy(own.offsets)
         psw = None if own.per_sample_weights is None else torch.from_numpy(own.per_sample_weights)
         routed = sb.route(idx, off, own.N, B, psw, synth.MEAN if mean else synth.SUM)
@@ -128,12 +129,12 @@ def _worker(rank, world, port, mode, out):
                                         own.indices, own.offsets, own.per_sample_weights,
                                         own.grad_output))
         if rank == 0:
-            out.put(_check(w, rb, shards, weighted, mean, optimizer, world))
+            out.put(_check(w, rb, shards, weighted, mean, optimizer, world, cyclic))
     finally:
         dist.destroy_process_group()
 
 
-def _check(w, rb, shards, weighted, mean, optimizer, world):
+def _check(w, rb, shards, weighted, mean, optimizer, world, cyclic):
     import oracle
     from sparse_embedding_bag_gb300 import shard as S
     T = len(ROWS)
@@ -164,18 +165,19 @@ def _check(w, rb, shards, weighted, mean, optimizer, world):
                     per_sample_weights=np.array(gpsw, np.float32) if gpsw else None, mean=mean)
     for r in range(world):
         sw, sm = shards[r][0], shards[r][1]
-        _, hsc, _, wo = S.local_tables(ROWS, DIMS, rb, r)
+        _, hsc, _, wo = S.local_tables(ROWS, DIMS, rb, r, world, cyclic)
+        own_rows = S.owned_rows(ROWS, rb, r, world, cyclic)
         for t in range(T):
-            lo, hi, D = rb[t, r], rb[t, r + 1], DIMS[t]
-            got = sw[wo[t]:wo[t] + (hi - lo) * D]
-            exp = ref_w[w.weights_offsets[t] + lo * D:w.weights_offsets[t] + hi * D]
+            D = DIMS[t]
+            got = sw[wo[t]:wo[t] + own_rows[t].size * D]
+            exp = ref_w[(w.weights_offsets[t] + own_rows[t][:, None] * D + np.arange(D)).reshape(-1)]
             exact = not (weighted or mean)
             if exact and not np.array_equal(got.view(np.uint32), exp.view(np.uint32)):
                 return f"weights of rank {r} table {t} differ"
             if not exact and not np.allclose(got, exp, rtol=1e-6, atol=1e-7):
                 return f"weights of rank {r} table {t} differ beyond rounding"
             if ref_m is not None:
-                em = ref_m[w.hash_size_cumsum[t] + lo:w.hash_size_cumsum[t] + hi]
+                em = ref_m[w.hash_size_cumsum[t] + own_rows[t]]
                 if not np.allclose(sm[hsc[t]:hsc[t + 1]], em, rtol=1e-6, atol=1e-9):
                     return f"state of rank {r} table {t} differs"
     if np.array_equal(ref_w, w.weights):
@@ -183,7 +185,8 @@ def _check(w, rb, shards, weighted, mean, optimizer, world):
     return "ok"
 
 
-@pytest.mark.parametrize("mode", ["sum", "weighted_mean", "adagrad"])
+@pytest.mark.parametrize("mode", ["sum", "weighted_mean", "adagrad", "cyclic_sum",
+                                  "cyclic_weighted_mean_adagrad"])
 def test_row_sharded_step_two_gloo_ranks(mode):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()

@@ -48,19 +48,20 @@ def gpu_bucketize(sh, w, W, mean, scales=True):
 
 
 @pytest.mark.parametrize("W,mode", [(1, "sum"), (8, "sum"), (8, "weighted"), (8, "mean"),
-                                    (3, "weighted_mean"), (64, "sum")])
+                                    (3, "weighted_mean"), (64, "sum"), (8, "cyclic_weighted_mean"),
+                                    (5, "cyclic_sum"), (256, "cyclic_sum")])
 def test_bucketize_parity(W, mode):
     rows = [5000, 300, 70, 1]
     w = batch(1, rows, [16, 8, 4, 4], 256, weighted="weighted" in mode, empty_share=0.2)
-    mean = "mean" in mode
-    rb = S.even_row_bounds(rows, W)  # the one-row table leaves W-1 ranks an empty range
-    sh = E.emb_shard_create(0, w.T, W, rb, w.B)
+    mean, cyclic = "mean" in mode, "cyclic" in mode
+    rb = S.even_row_bounds(rows, W)  # the one-row table leaves W-1 ranks no rows
+    sh = E.emb_shard_create_cyclic(0, w.T, W, rows, w.B) if cyclic else E.emb_shard_create(0, w.T, W, rb, w.B)
     try:
         so, si, ss, sc = gpu_bucketize(sh, w, W, mean)
     finally:
         E.emb_shard_destroy(sh)
     eo, ei, es, ec = oracle.bucketize(w.T, w.B, rb, w.indices, w.offsets,
-                                      per_sample_weights=w.per_sample_weights, mean=mean)
+                                      per_sample_weights=w.per_sample_weights, mean=mean, cyclic=cyclic)
     assert np.array_equal(sc, ec)
     assert np.array_equal(so, eo)
     assert np.array_equal(si, ei)
@@ -169,7 +170,7 @@ def test_merge_reports_inconsistent_offsets():
         E.emb_shard_destroy(sh)
 
 
-def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30):
+def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30, cyclic=False):
     """W ranks on one GPU: every rank's bucketize, the all-to-all as device copies,
     every owner's merge, backward (and forward) on its own plan. Returns the
     unsharded weights, state and every rank's forward output."""
@@ -183,7 +184,7 @@ def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30):
     need_scales = weighted or mean
     sends = []
     for s, src in enumerate(sources):
-        sh = E.emb_shard_create(0, T, W, rb, B)
+        sh = E.emb_shard_create_cyclic(0, T, W, rows, B) if cyclic else E.emb_shard_create(0, T, W, rb, B)
         try:
             so = torch.empty((W, T * B + 1), dtype=torch.int64, device="cuda")
             si = torch.empty(max(src.N, 1), dtype=torch.int64, device="cuda")
@@ -208,8 +209,9 @@ def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30):
         ri = torch.cat([p[0] for p in pieces])
         rs = torch.cat([p[1] for p in pieces]) if need_scales else None
         n = int(ri.numel())
-        local, hsc, Do, wo = S.local_tables(rows, dims, rb, r)
-        sh = E.emb_shard_create(0, T, W, rb, B)
+        local, hsc, Do, wo = S.local_tables(rows, dims, rb, r, W, cyclic)
+        own = S.owned_rows(rows, rb, r, W, cyclic)
+        sh = E.emb_shard_create(0, T, W, rb, B)  # merge does not depend on the map
         plan = E.emb_bwd_plan(0, T, hsc, Do, wo, None, synth.F32, synth.F32, max(n, 1), W * B, 0, 0)
         try:
             mo = torch.empty(T * W * B + 1, dtype=torch.int64, device="cuda")
@@ -217,13 +219,11 @@ def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30):
             ms = torch.empty(max(n, 1), dtype=torch.float32, device="cuda") if need_scales else None
             E.emb_shard_merge(sh, ro, ri if n else mi, rs if (n or not need_scales) else ms, n, B, mo, mi, ms)
             assert E.emb_shard_status(sh) == E.EMB_OK
-            lo, hi = rb[:, r], rb[:, r + 1]
-            wl = torch.from_numpy(np.concatenate(
-                [model.weights[model.weights_offsets[t] + lo[t] * dims[t]:
-                               model.weights_offsets[t] + hi[t] * dims[t]] for t in range(T)])).cuda()
+            gidx = [(model.weights_offsets[t] + own[t][:, None] * dims[t] + np.arange(dims[t])).reshape(-1)
+                    for t in range(T)]
+            wl = torch.from_numpy(np.concatenate([model.weights[g] for g in gidx])).cuda()
             ml = None if mom_full is None else torch.from_numpy(np.concatenate(
-                [model.momentum[model.hash_size_cumsum[t] + lo[t]:model.hash_size_cumsum[t] + hi[t]]
-                 for t in range(T)])).cuda()
+                [model.momentum[model.hash_size_cumsum[t] + own[t]] for t in range(T)])).cuda()
             out = torch.zeros((W * B, int(np.sum(dims))), dtype=torch.float32, device="cuda")
             if n:
                 E.emb_bag_fwd(plan, wl, mi, mo, n, W * B, ms, E.EMB_POOL_SUM, out, 0)
@@ -237,23 +237,24 @@ def emulated_step(rows, dims, B, W, optimizer, weighted, mean, seed=30):
             wl_np = wl.cpu().numpy()
             for t in range(T):
                 D = int(dims[t])
-                weights_full[model.weights_offsets[t] + lo[t] * D:model.weights_offsets[t] + hi[t] * D] = \
-                    wl_np[wo[t]:wo[t] + (hi[t] - lo[t]) * D]
+                weights_full[gidx[t]] = wl_np[wo[t]:wo[t] + own[t].size * D]
                 if ml is not None:
-                    mom_full[model.hash_size_cumsum[t] + lo[t]:model.hash_size_cumsum[t] + hi[t]] = \
-                        ml.cpu().numpy()[hsc[t]:hsc[t + 1]]
+                    mom_full[model.hash_size_cumsum[t] + own[t]] = ml.cpu().numpy()[hsc[t]:hsc[t + 1]]
         finally:
             E.emb_plan_destroy(plan)
             E.emb_shard_destroy(sh)
     return model, sources, weights_full, mom_full, fwd
 
 
-@pytest.mark.parametrize("optimizer,weighted,mean", [(synth.SGD, False, False),
-                                                     (synth.SGD, True, True),
-                                                     (synth.ROWWISE_ADAGRAD, True, False)])
-def test_emulated_sharded_step_equals_unsharded(optimizer, weighted, mean):
+@pytest.mark.parametrize("optimizer,weighted,mean,cyclic", [(synth.SGD, False, False, False),
+                                                            (synth.SGD, True, True, False),
+                                                            (synth.ROWWISE_ADAGRAD, True, False, False),
+                                                            (synth.SGD, False, False, True),
+                                                            (synth.ROWWISE_ADAGRAD, True, True, True)])
+def test_emulated_sharded_step_equals_unsharded(optimizer, weighted, mean, cyclic):
     rows, dims, B, W = [3000, 200, 57], [32, 8, 64], 128, 4
-    model, sources, got_w, got_m, fwd = emulated_step(rows, dims, B, W, optimizer, weighted, mean)
+    model, sources, got_w, got_m, fwd = emulated_step(rows, dims, B, W, optimizer, weighted, mean,
+                                                      cyclic=cyclic)
     T = len(rows)
     # the unsharded step on the global batch (bag (t, s*B + b) = source s's bag (t, b))
     gidx, goff, gpsw = [], [0], []
