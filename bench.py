@@ -41,7 +41,7 @@ DESCR = {
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant kernel, from the ncu captures summarised under profiles/; a workload
 # without an entry for the current kernels reports null.
-TRAFFIC = {("dlrm", "reduce_update"): 21_140_224}  # profiles/k_reduce_dlrm.md
+TRAFFIC = {("dlrm", "reduce_update"): 21_139_712}  # profiles/k_reduce_dlrm.md
 
 
 def parse():
@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--op", default="bwd", choices=["bwd", "fwd", "shard"],
                     help="bwd: backward + update (the headline); fwd: forward pooled lookup; "
                          "shard: row-sharded step of one rank (W ranks emulated on one GPU)")
+    ap.add_argument("--variant", default="update", choices=["update", "dense", "adagrad", "sr"],
+                    help="bwd: update = the workload's optimizer; dense = dense-gradient mode; "
+                         "adagrad = elementwise Adagrad; sr = the update with stochastic rounding")
     ap.add_argument("--shards", type=int, default=8, help="ranks W of --op shard")
     ap.add_argument("--shard-map", default="cyclic", choices=["cyclic", "ranges"],
                     help="row map of --op shard: rows modulo W, or contiguous ranges")
@@ -79,9 +82,11 @@ def host_arrays(w):
     return conv(w.indices), conv(w.offsets), conv(w.grad_output), conv(w.per_sample_weights)
 
 
-def algorithmic_bytes(w, indices, offsets):
+def algorithmic_bytes(w, indices, offsets, variant="update"):
     """Minimal bytes of one step: int64 indices, the gradient row read per lookup,
-    and one read + one write of every unique row (and its fp32 state for Adagrad).
+    and one read + one write of every unique row (and its fp32 state for Adagrad:
+    8 bytes per row row-wise, 8 per element elementwise). The dense-gradient mode
+    writes every unique row once and clears the whole weights-sized buffer.
     Returns (step bytes, reduce-kernel bytes, unique rows)."""
     from sparse_embedding_bag_gb300 import synth
     lengths = np.diff(offsets)
@@ -92,8 +97,14 @@ def algorithmic_bytes(w, indices, offsets):
     gsize = 4 if w.grad_dtype == synth.F32 else 2
     wsize = 4 if w.weight_dtype == synth.F32 else 2
     grad_bytes = int(w.dims[t_of_lookup].astype(np.int64).sum()) * gsize
-    row_bytes = int(w.dims[t_of_row].astype(np.int64).sum()) * 2 * wsize
+    row_elems = int(w.dims[t_of_row].astype(np.int64).sum())
+    row_bytes = row_elems * 2 * wsize
     state = 8 * uniq.size if w.optimizer == synth.ROWWISE_ADAGRAD else 0
+    if variant == "adagrad":
+        state = 8 * row_elems
+    if variant == "dense":
+        reduce_bytes = grad_bytes + row_elems * wsize
+        return 8 * indices.size + reduce_bytes + int(np.asarray(w.weights).size) * wsize, reduce_bytes, int(uniq.size)
     reduce_bytes = grad_bytes + row_bytes + state
     return 8 * indices.size + reduce_bytes, reduce_bytes, int(uniq.size)
 
@@ -161,20 +172,32 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def cpu_baseline(w, budget_s):
+def cpu_baseline(w, budget_s, variant="update"):
     """The oracle, as it stands (single thread), on the same workload for ~budget_s seconds."""
     import oracle
     from sparse_embedding_bag_gb300 import synth
     indices, offsets, grad, psw = host_arrays(w)
     n_done, el, runs = 0, 0.0, 0
+    wts = np.asarray(w.weights)
     while el < budget_s:
-        weights = np.array(w.weights, copy=True)
+        weights = np.array(wts, copy=True)
         mom = None if w.momentum is None else np.array(w.momentum, copy=True)
+        kw = dict(per_sample_weights=psw, mean=(w.pooling == synth.MEAN), nobag=w.nobag,
+                  grad_dtype=w.grad_dtype)
         t1 = time.perf_counter()
-        oracle.backward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, weights,
-                        indices, offsets, grad, optimizer=w.optimizer, lr=w.lr, eps=w.eps,
-                        momentum=mom, momentum_offsets=w.momentum_offsets, per_sample_weights=psw,
-                        mean=(w.pooling == synth.MEAN), nobag=w.nobag, grad_dtype=w.grad_dtype)
+        if variant == "dense":
+            oracle.dense_grad(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, wts.size,
+                              indices, offsets, grad, out_dtype=w.weight_dtype, **kw)
+        elif variant == "adagrad":
+            m = np.zeros(wts.size, np.float32)
+            oracle.backward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, weights,
+                            indices, offsets, grad, optimizer=oracle.ADAGRAD, lr=w.lr, eps=w.eps,
+                            momentum=m, **kw)
+        else:
+            oracle.backward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets, weights,
+                            indices, offsets, grad, optimizer=w.optimizer, lr=w.lr, eps=w.eps,
+                            momentum=mom, momentum_offsets=w.momentum_offsets,
+                            stochastic_rounding=(1, runs) if variant == "sr" else None, **kw)
         el += time.perf_counter() - t1
         n_done += indices.size
         runs += 1
@@ -429,6 +452,26 @@ def run_shard(args):
     dom = max(stages, key=lambda k: stages[k][0])
     ach = stages[dom][1] / (stages[dom][0] * 1e-3) / 1e9
     ms = ms_b + ms_m + ms_r
+    cpu = None
+    if not args.no_cpu_baseline:
+        # the oracle on the same step: rank 0's bucketize, the owner's merge and backward
+        parts = [oracle.bucketize(T, B, rb, x.indices, x.offsets, cyclic=cyclic) for x in srcs]
+        el, runs = 0.0, 0
+        while el < min(args.cpu_seconds, 10.0) or runs == 0:
+            t1 = time.perf_counter()
+            oracle.bucketize(T, B, rb, srcs[0].indices, srcs[0].offsets, cyclic=cyclic)
+            ro_h = np.stack([p[0][r] for p in parts])
+            ri_h = np.concatenate([p[1][int(p[3][:r].sum()):int(p[3][:r].sum()) + int(p[3][r])] for p in parts])
+            mo_h, mi_h, _ = oracle.merge(T, B, W, ro_h, ri_h, np.ones(ri_h.size, np.float32))
+            wl_h = wl.cpu().numpy().copy()
+            ml_h = np.zeros(int(hsc[-1]), np.float32)
+            oracle.backward(T, W * B, hsc, Do, wo, wl_h, mi_h, mo_h, grad.cpu().numpy(),
+                            optimizer=w.optimizer, lr=w.lr, eps=w.eps, momentum=ml_h)
+            el += time.perf_counter() - t1
+            runs += 1
+        cpu = {"value": int(recv_counts.sum()) * runs / el, "unit": "lookups/s", "cores": 1,
+               "kind": "oracle", "sample": f"{runs} step(s): rank 0's bucketize, owner {r}'s merge and "
+                                           f"backward, {el:.1f} s, single-threaded"}
     print(json.dumps({
         "metric": "row-sharded embedding step, W ranks (exchange kernels + the most loaded owner's "
                   "backward, communication excluded): all ranks' lookups/sec",
@@ -443,7 +486,7 @@ def run_shard(args):
         "stage_ms": {"bucketize": ms_b, "merge": ms_m, "backward_owner": ms_r},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak, "traffic": None},
-        "cpu_baseline": None,
+        "cpu_baseline": cpu,
         # bucketize: count, three scan phases, scatter; merge: bases, copy; backward:
         # histogram, radix passes, run-length, reduce
         "gpu_launches": K * (5 + 2 + 3 + -(-max(int(hsc[-1] - 1).bit_length(), 1) // 8)),
@@ -479,15 +522,35 @@ def main():
     E.load()
 
     w = make_workload(args.workload, rank, f"cuda:{local}")
+    variant = args.variant
+    if variant == "sr" and w.weight_dtype == synth.F32:
+        raise SystemExit("--variant sr needs a workload with fp16 / bf16 weights (mixed, large)")
+    if variant == "adagrad" and w.nobag:
+        raise SystemExit("--variant adagrad needs a pooled workload")
     indices_h, offsets_h, grad_h, psw_h = host_arrays(w)
-    step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, indices_h, offsets_h)
+    step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, indices_h, offsets_h, variant)
     dw = dev.to_device(w, f"cuda:{local}")
-    plan = dev.make_plan(w, device_index=local, flags=E.EMB_FLAG_NO_PDL if args.no_pdl else 0)
+    flags = (E.EMB_FLAG_NO_PDL if args.no_pdl else 0) | (E.EMB_FLAG_STOCHASTIC_ROUNDING if variant == "sr" else 0)
+    plan = dev.make_plan(w, device_index=local, flags=flags)
     path = {"auto": E.EMB_NOBAG_AUTO, "sorted": E.EMB_NOBAG_SORTED, "atomic": E.EMB_NOBAG_ATOMIC}[args.path]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=f"cuda:{local}")
+    dense_buf = torch.empty_like(dw.weights) if variant == "dense" else None
+    ew_state = torch.zeros(dw.weights.numel(), dtype=torch.float32, device=f"cuda:{local}") \
+        if variant == "adagrad" else None
 
     def call():
-        dev.step(plan, dw, path=path)
+        if variant == "dense":
+            if w.nobag:
+                E.emb_nobag_bwd_dense_grad(plan, dense_buf, dw.indices, dw.offsets, w.N, w.B,
+                                           dw.grad_output)
+            else:
+                E.emb_bag_bwd_dense_grad(plan, dense_buf, dw.indices, dw.offsets, w.N, w.B,
+                                         dw.per_sample_weights, dw.grad_output, w.pooling)
+        elif variant == "adagrad":
+            E.emb_bag_bwd_adagrad(plan, dw.weights, ew_state, dw.indices, dw.offsets, w.N, w.B,
+                                  dw.per_sample_weights, dw.grad_output, w.pooling, w.lr, w.eps)
+        else:
+            dev.step(plan, dw, path=path)
 
     for _ in range(max(args.warmup, 3)):
         call()
@@ -632,6 +695,9 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": DESCR[args.workload], "N": n_local, "unique_rows": uniq,
+                   "variant": {"update": "the workload's optimizer", "dense": "dense-gradient mode",
+                               "adagrad": "elementwise Adagrad",
+                               "sr": "the workload's optimizer, stochastic rounding"}[variant],
                    "l2": "256 MB buffer written between timed steps", "cuda_graph": use_graph, "pdl": not args.no_pdl,
                    "parallelism": f"{world} independent shard(s), no collective"},
         "hbm_gbs": step_bytes / (ms_job * 1e-3) / 1e9,
@@ -650,7 +716,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, variant)
     E.emb_plan_destroy(plan)
     if rank == 0:
         print(json.dumps(result, default=float))
