@@ -431,9 +431,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += W0;
       k1 += W1;
     }
-    const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
-    const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)M0 * c.x, p1 = (uint64_t)M1 * c.z;  // one wide multiply each
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                   (uint32_t)p0);
   }
   return c;
 }
@@ -447,16 +447,19 @@ __device__ __forceinline__ uint16_t sr_bf16(float x, uint32_t r) {
 }
 
 // fp32 x to fp16 bits: the neighbour toward zero, moved one ulp away from zero
-// with probability (|x| - |lo|) / ulp, compared on 24 random bits (exact in fp32).
+// with probability (|x| - |lo|) / ulp, compared on 24 random bits. Both steps
+// are exact in fp32: |x| - |lo| by Sterbenz (|lo| <= |x| < |lo| + ulp <= 2|lo|,
+// or lo = 0), and the division by ulp = 2^(max(e,1) - 25) (e the exponent field
+// of lo) is a multiplication by its exact power-of-two reciprocal. Beyond the
+// largest finite value (hi would be inf) the result stays at the largest finite.
 __device__ __forceinline__ uint16_t sr_half(float x, uint32_t r) {
   const __half h = __float2half_rz(x);
   const uint16_t lo = *reinterpret_cast<const uint16_t*>(&h);
-  if ((lo & 0x7C00u) == 0x7C00u) return lo;  // inf / nan
-  const uint16_t hi = (uint16_t)(lo + 1);
-  const float a = fabsf(__half2float(h));
-  const float b = fabsf(__half2float(*reinterpret_cast<const __half*>(&hi)));
-  const float frac = __fdiv_rn(fabsf(x) - a, b - a);
-  return (r >> 8) < (uint32_t)(frac * 16777216.0f) ? hi : lo;
+  if ((lo & 0x7C00u) == 0x7C00u || (lo & 0x7FFFu) == 0x7BFFu) return lo;  // inf / nan / saturated
+  const uint32_t e = max((uint32_t)(lo >> 10) & 0x1Fu, 1u);
+  const float inv_ulp = __uint_as_float((127u + 25u - e) << 23);
+  const float frac = (fabsf(x) - fabsf(__half2float(h))) * inv_ulp;
+  return (r >> 8) < (uint32_t)(frac * 16777216.0f) ? (uint16_t)(lo + 1) : lo;
 }
 
 // ---- 4-element vector loads/stores of the storage types, as fp32.
