@@ -74,12 +74,25 @@ struct Unroll {
 constexpr uint32_t kStaticSlice = 256;
 constexpr uint32_t kMinDynSlice = 64;
 
+// Whether the gather loads the next step's sorted values while the current
+// step's gradient rows are in flight (one dependent load less per step, for a
+// few more registers). Measured on GB300: pays for unweighted pooled lookups of
+// one team shape (DLRM-like reduce 33.5 -> 32.0 us, the large skewed one 7.19 ->
+// 6.36 ms); with several team shapes, or 64-bit (weighted) values, it spills,
+// and unpooled rows (whole-warp lookups of chunked wide rows) lost 12 %.
+template <int VK, bool MULTI>
+struct PrefetchVals {
+  static constexpr bool value = !MULTI && VK == VK_BAG;
+};
+
 // Minimum resident blocks per SM, by vectors per lane (register budget).
-// Measured on GB300: with several team shapes (more loop state), 2 vectors per
-// lane run best at 3 blocks (80 registers) rather than 4 with spills.
-template <int KV, bool MULTI>
+// Measured on GB300: 2 vectors per lane run best at 3 blocks (80 registers)
+// with several team shapes (more loop state) or with the prefetch above, and at
+// 4 blocks (64 registers) otherwise.
+template <int KV, bool MULTI, int VK>
 struct MinBlocks {
-  static constexpr int value = KV == 1 ? 4 : (KV == 2 ? (MULTI ? 3 : 4) : (KV == 4 ? 2 : 1));
+  static constexpr int value =
+      KV == 1 ? 4 : (KV == 2 ? ((MULTI || PrefetchVals<VK, MULTI>::value) ? 3 : 4) : (KV == 4 ? 2 : 1));
 };
 
 // Sum over sorted positions [jb, je) of one run into acc by a team of lanes.
@@ -87,7 +100,8 @@ struct MinBlocks {
 // li = lane in group covering vectors li, li+Lg, ...), P groups gather P
 // lookups per step, UNR steps are issued before any result is consumed.
 // `steps` is warp-uniform (teams of one warp may hold runs of different length).
-template <int VK, typename grad_t, int KV>
+// PF: the sorted values of step s+1 are loaded right after the rows of step s.
+template <int VK, typename grad_t, int KV, bool PF>
 __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape& rs, uint32_t jb,
                                             uint32_t je, uint32_t steps, uint32_t P, uint32_t g,
                                             uint32_t li, float4 (&acc)[KV]) {
@@ -113,6 +127,14 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
   }
 #pragma unroll
   for (int k = 0; k < KV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  V vn[UNR];
+  if constexpr (PF) {
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const uint32_t j = jb + u * P + g;
+      vn[u] = (steps > 0 && j < je) ? vals[j] : (V)0;
+    }
+  }
   for (uint32_t s = 0; s < steps; ++s) {
     V v[UNR];
     bool ok[UNR];
@@ -120,7 +142,8 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
     for (int u = 0; u < UNR; ++u) {
       const uint32_t j = jb + (s * UNR + u) * P + g;
       ok[u] = j < je;
-      v[u] = ok[u] ? vals[j] : (V)0;
+      if constexpr (PF) v[u] = vn[u];
+      else v[u] = ok[u] ? vals[j] : (V)0;
     }
     typename Vec4<grad_t>::Raw x[UNR][KV];  // loaded bits, widened when added
     float scale[UNR];
@@ -133,6 +156,13 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
       for (int k = 0; k < KV; ++k)
         x[u][k] = (ok[u] && on[k]) ? Vec4<grad_t>::load_raw(reinterpret_cast<const grad_t*>(row + col[k]))
                                    : Vec4<grad_t>::zero_raw();
+    }
+    if constexpr (PF) {
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const uint32_t j = jb + ((s + 1) * UNR + u) * P + g;
+        vn[u] = (s + 1 < steps && j < je) ? vals[j] : (V)0;
+      }
     }
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -406,7 +436,7 @@ __device__ __forceinline__ bool piece_arrive(const ReduceArgs& a, const RowShape
 // MULTI: the tables form several segments of different team shapes (see
 // phase 2); without it, one shape serves every table and phase 2 is one sweep.
 template <typename emb_t, typename grad_t, int OPT, int VK, int KV, bool MULTI>
-__global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduce(ReduceArgs a) {
+__global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_reduce(ReduceArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* s_hsc = reinterpret_cast<uint32_t*>(smem);  // [T+1]
   int32_t* s_Do = reinterpret_cast<int32_t*>(s_hsc + a.T + 1);  // [T+1]
@@ -487,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
         const uint32_t jb = lr.start + (max(a0, p0) - p0), je = lr.start + (min(b0, p1) - p0);
         const uint32_t steps = (je - jb + Pg * UNR - 1) / (Pg * UNR);
         float4 acc[KV];
-        team_gather<VK, grad_t, KV>(a, rs, jb, je, steps, Pg, g, li, acc);
+        team_gather<VK, grad_t, KV, PrefetchVals<VK, MULTI>::value>(a, rs, jb, je, steps, Pg, g, li, acc);
         team_fold<KV>(acc, 1u << rs.lg, 32);
         if (whole) {  // long runs: the row is read after the gather (registers)
           load_row<emb_t, OPT, KV>(a, rs, true, g, li, wv);
@@ -539,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI>::value) k_reduc
     const uint32_t my_steps = (end - start + Pt * UNR - 1) / (Pt * UNR);
     const uint32_t steps = __reduce_max_sync(0xffffffffu, my_steps);
     float4 acc[KV];
-    team_gather<VK, grad_t, KV>(a, rs, start, end, steps, Pt, g, li, acc);
+    team_gather<VK, grad_t, KV, PrefetchVals<VK, MULTI>::value>(a, rs, start, end, steps, Pt, g, li, acc);
     team_fold<KV>(acc, 1u << rs.lg, Lt);
     update_row<emb_t, OPT, KV>(a, rs, active, g, li, tl, Lt, acc, wv, m_old);
   };
