@@ -91,8 +91,8 @@ struct emb_plan {
   uint32_t seq = 0;
   int reduce_grid[3][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};  // [optimizer][value kind]
   int64_t w_extent = 0;  // elements of the weights layout: max over t of offset + rows * D
-  // Blocks that fit on the GPU at once: sort pass [large tiles][wide payload], k_runs [split].
-  int pass_cap[2][2] = {{0, 0}, {0, 0}};
+  // Blocks that fit on the GPU at once: sort pass [tile class][wide payload], k_runs [split].
+  int pass_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};  // [pass tile class][wide values]
   int runs_cap[2] = {0, 0};
   int fwd_grid[3] = {0, 0, 0};  // forward kernel grid per output type (0: not set up yet)
   cudaStream_t last_stream = nullptr;
@@ -183,7 +183,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   const uint32_t epoch = ++p->seq * 8u;
   if (p->seq >= (1u << 28)) p->seq = 0;  // epochs stay distinct from the zero-initialised words
   const DecodeArgs d = decode_args(p, indices, offsets, psw, N, B, mean);
-  const int tile = (int)sort_tile_for(N);
+  const int tile = (int)sort_tile_for(N), ptile = (int)pass_tile_for(N);
   const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
   const bool wide = vk == VK_BAG_SCALED;
   const LookbackCfg lb0{p->status, epoch, kSpinLimit, (p->flags & EMB_FLAG_DEBUG_FORCE_TIMEOUT) ? 1u : 0u};
@@ -209,8 +209,8 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_out = p->vals[out];
     pa.pass = pass;
     pa.shift = pass * kRadixBits;
-    pa.ordered = (N + tile - 1) / tile <= p->pass_cap[tile == kThreads * 4 ? 0 : 1][wide ? 1 : 0];
-    EMB_CUDA(launch_sort_pass(pa, wide, tile, s, pdl));
+    pa.ordered = (N + ptile - 1) / ptile <= p->pass_cap[pass_tile_class(ptile)][wide ? 1 : 0];
+    EMB_CUDA(launch_sort_pass(pa, wide, ptile, s, pdl));
   }
   const int fin = (passes - 1) & 1;
   EMB_TRY(record(p, 2, s));
@@ -497,9 +497,10 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   }
   if (e == cudaSuccess) e = sort_configure(p->props);
   if (e == cudaSuccess) {
-    for (int big = 0; big < 2; ++big)
+    const int tiles[3] = {kThreads * 4, kThreads * 8, kThreads * 16};
+    for (int c = 0; c < 3; ++c)
       for (int wide = 0; wide < 2; ++wide)
-        p->pass_cap[big][wide] = sort_pass_capacity(wide != 0, big ? kThreads * 16 : kThreads * 4, p->props.sms);
+        p->pass_cap[c][wide] = sort_pass_capacity(wide != 0, tiles[c], p->props.sms);
     for (int opt = 0; opt < 2; ++opt)
       p->runs_cap[opt] = runs_capacity((int)p->split[opt].segs.size() - 1, p->props.sms);
   }

@@ -564,7 +564,9 @@ inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, size_t s
 }
 
 // sort.cu
-size_t sort_tile_for(int64_t N);  // lookups per block for hist and the passes
+size_t sort_tile_for(int64_t N);  // lookups per block of the histogram kernel
+size_t pass_tile_for(int64_t N);  // lookups per block of the radix passes: 1024, 2048 or 4096
+int pass_tile_class(int tile);    // 0, 1, 2 for those
 // first_kind: the ValueKind of the pairs to write, or -1 to only check indices and offsets.
 cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s, bool pdl);
 cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl);
