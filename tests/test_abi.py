@@ -97,3 +97,42 @@ def test_header_declares_status_codes_used_by_binding():
         assert name in text
     assert "EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u" in text
     assert E.EMB_FLAG_DEBUG_FORCE_TIMEOUT == 0x100
+
+
+def _shard(lib, T=2, W=2, rb=((0, 5, 10), (0, 3, 7)), max_B=4, out=True, cyclic=False):
+    p = ctypes.c_void_p()
+    if cyclic:
+        a = np.ascontiguousarray(rb, np.int64)
+        st = lib.emb_shard_create_cyclic(ctypes.byref(p) if out else None, 0, T, W, a.ctypes.data, max_B)
+    else:
+        a = np.ascontiguousarray(rb, np.int64)
+        st = lib.emb_shard_create(ctypes.byref(p) if out else None, 0, T, W, a.ctypes.data, max_B)
+    return st, p
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=0),
+    dict(W=0),
+    dict(W=300, rb=[[0] * 300 + [10], [0] * 300 + [7]]),   # more than 256 ranks
+    dict(rb=((1, 5, 10), (0, 3, 7))),                        # ranges must start at row 0
+    dict(rb=((0, 6, 5), (0, 3, 7))),                         # decreasing bounds
+    dict(rb=((0, 0, 0), (0, 3, 7))),                         # a table without rows
+    dict(max_B=0),
+    dict(max_B=1 << 29),                                     # W * T * max_B >= 2^31
+    dict(out=False),
+    dict(cyclic=True, rb=(10, 0)),                           # cyclic: a table without rows
+])
+def test_shard_create_rejects_bad_arguments_without_cuda(lib, kw):
+    st, p = _shard(lib, **kw)
+    assert st == E.EMB_ERR_INVALID_ARG
+    assert not p.value
+
+
+def test_shard_and_rounding_calls_reject_null_handles(lib):
+    assert lib.emb_shard_bucketize(None, None, None, 0, 1, None, 0, None, None, None, None, None) == \
+        E.EMB_ERR_INVALID_ARG
+    assert lib.emb_shard_merge(None, None, None, None, 0, 1, None, None, None, None) == E.EMB_ERR_INVALID_ARG
+    assert lib.emb_shard_status(None) == E.EMB_ERR_INVALID_ARG
+    assert lib.emb_shard_destroy(None) == E.EMB_OK
+    assert lib.emb_plan_set_rounding(None, 1, 2) == E.EMB_ERR_INVALID_ARG
+    assert lib.emb_plan_get_rounding(None, None, None) == E.EMB_ERR_INVALID_ARG
