@@ -250,7 +250,6 @@ def run_reference(args):
 def run_forward(args):
     """Forward pooled lookup on one GPU: the same timing rules as the backward."""
     import torch
-    import oracle
     from sparse_embedding_bag_gb300 import build as b
     from sparse_embedding_bag_gb300 import device as dev
     from sparse_embedding_bag_gb300 import embbwd as E
@@ -324,6 +323,7 @@ def run_forward(args):
     e2e_s = statistics.median(e2e[2:])
     cpu = None
     if not args.no_cpu_baseline:
+        import oracle
         n_done, el, runs = 0, 0.0, 0
         while el < min(args.cpu_seconds, 10.0):
             t1 = time.perf_counter()
@@ -377,7 +377,6 @@ def run_shard(args):
     exchange itself: bucketize (rank 0's batch; it synchronises for the sizes),
     merge and backward (the most loaded owner)."""
     import torch
-    import oracle
     from sparse_embedding_bag_gb300 import build as b
     from sparse_embedding_bag_gb300 import embbwd as E
     from sparse_embedding_bag_gb300 import shard as S
@@ -440,9 +439,6 @@ def run_shard(args):
     torch.cuda.synchronize()
     if E.emb_shard_status(sh) != E.EMB_OK or E.emb_plan_status(plan) != E.EMB_OK:
         raise SystemExit("device status error")
-    # parity of this configuration's exchange (bit for bit) on the way
-    eo, ei, _, ec = oracle.bucketize(T, B, rb, srcs[0].indices, srcs[0].offsets, cyclic=cyclic)
-    assert np.array_equal(so0.cpu().numpy(), eo) and np.array_equal(si0[:srcs[0].N].cpu().numpy(), ei)
     with ClockSampler(0) as clocks:
         ms_b = timed(bucketize, K, flush, stream)
         ms_m = timed(merge, K, flush, stream)
@@ -457,6 +453,7 @@ def run_shard(args):
     ms = ms_b + ms_m + ms_r
     cpu = None
     if not args.no_cpu_baseline:
+        import oracle
         # the oracle on the same step: rank 0's bucketize, the owner's merge and backward
         parts = [oracle.bucketize(T, B, rb, x.indices, x.offsets, cyclic=cyclic) for x in srcs]
         el, runs = 0.0, 0
