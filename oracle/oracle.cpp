@@ -70,6 +70,7 @@ double half_to_double(uint16_t h) {
 uint16_t double_to_half(double x) {
   const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
   if (std::isnan(x)) return sign | 0x7E00;
+  if (std::isinf(x)) return sign | 0x7C00;
   const double a = std::fabs(x);
   if (a == 0.0) return sign;
   if (a < std::ldexp(1.0, -14)) {
@@ -99,6 +100,7 @@ double bf16_to_double(uint16_t h) {
 uint16_t double_to_bf16(double x) {
   const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
   if (std::isnan(x)) return sign | 0x7FC0;
+  if (std::isinf(x)) return sign | 0x7F80;
   const double a = std::fabs(x);
   if (a == 0.0) return sign;
   if (a < std::ldexp(1.0, -126)) {

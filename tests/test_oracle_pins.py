@@ -356,7 +356,7 @@ def test_half_conversion_vs_numpy(oracle_mod):
     rng = np.random.default_rng(0)
     xs = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-9, 6, 3000),
                          [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e-8, 2.0 ** -24, 2.0 ** -25,
-                          3 * 2.0 ** -26, 2.0 ** -14 - 2.0 ** -26]])
+                          3 * 2.0 ** -26, 2.0 ** -14 - 2.0 ** -26, np.inf, -np.inf, 1e300, -1e300]])
     for x in xs:
         assert oracle_mod.double_to_half_bits(x) == int(np.float64(x).astype(np.float16).view(np.uint16)), x
     for h in range(0, 0x7C00, 37):
@@ -372,7 +372,8 @@ def test_half_ties_to_even(oracle_mod):
 def test_bf16_conversion(oracle_mod):
     import torch
     rng = np.random.default_rng(1)
-    xs = (rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000)).astype(np.float32)
+    xs = np.concatenate([(rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000)),
+                         [np.inf, -np.inf, 3.4e38, -3.4e38]]).astype(np.float32)
     ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     for x, r in zip(xs, ref):
         assert oracle_mod.double_to_bf16_bits(float(x)) == int(r), x

@@ -117,3 +117,17 @@ def test_backward_sr_stores_a_bracketing_value(oracle_mod, wdt):
                         w.indices, w.offsets, w.grad_output, optimizer=oracle_mod.SGD, lr=0.03,
                         stochastic_rounding=(1234, 8))
     assert not np.array_equal(got, got2)
+
+
+def test_sr_half_saturates_and_passes_inf(oracle_mod):
+    # beyond the largest finite fp16 (65504 = 0x7BFF) the neighbour away from zero
+    # would be infinity: the update stays at the largest finite value
+    for r in (0, 1 << 8, 0xFFFFFF00):
+        assert oracle_mod.sr_half_bits(70000.0, r) == 0x7BFF
+        assert oracle_mod.sr_half_bits(-1e9, r) == 0xFBFF
+        assert oracle_mod.sr_half_bits(65504.0, r) == 0x7BFF
+        assert oracle_mod.sr_half_bits(float("inf"), r) == 0x7C00
+        assert oracle_mod.sr_half_bits(float("-inf"), r) == 0xFC00
+    # just below 65504 the rule still rounds up with the dropped fraction
+    assert oracle_mod.sr_half_bits(65500.0, 0) == 0x7BFF  # (65500 - 65472) / 32 > 0: r = 0 rounds up
+    assert oracle_mod.sr_half_bits(65500.0, 0xFFFFFF00) == 0x7BFE
