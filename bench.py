@@ -175,10 +175,42 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def host_subset(w, tables=2):
+    """A workload drawn on the device, cut to its first `tables` tables on the host
+    (tables are independent, so the oracle's rate per lookup carries over)."""
+    import dataclasses
+    T2 = min(tables, w.T)
+    off = w.offsets[:T2 * w.B + 1].cpu().numpy()
+    n2 = int(off[-1])
+    wend = int(w.weights_offsets[T2 - 1]) + int(w.rows[T2 - 1]) * int(w.dims[T2 - 1])
+    conv = lambda x: None if x is None else x.cpu().numpy()
+    weights = w.weights[:wend].cpu()
+    weights = weights.view(torch_int16()).numpy().view(np.uint16) if str(weights.dtype) == "torch.bfloat16" \
+        else weights.numpy()
+    return dataclasses.replace(
+        w, T=T2, rows=w.rows[:T2], dims=w.dims[:T2], hash_size_cumsum=w.hash_size_cumsum[:T2 + 1],
+        D_offsets=w.D_offsets[:T2 + 1], weights_offsets=w.weights_offsets[:T2],
+        momentum_offsets=None if w.momentum_offsets is None else w.momentum_offsets[:T2],
+        indices=w.indices[:n2].cpu().numpy(), offsets=off,
+        grad_output=w.grad_output[:, :int(w.D_offsets[T2])].contiguous().cpu().numpy(),
+        weights=weights,
+        momentum=None if w.momentum is None else w.momentum[:int(w.hash_size_cumsum[T2])].cpu().numpy(),
+        per_sample_weights=None if w.per_sample_weights is None else conv(w.per_sample_weights[:n2]))
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 def cpu_baseline(w, budget_s, variant="update"):
-    """The oracle, as it stands (single thread), on the same workload for ~budget_s seconds."""
+    """The oracle, as it stands (single thread), on the same workload for ~budget_s seconds
+    (for a workload drawn on the device, on its first two tables)."""
     import oracle
     from sparse_embedding_bag_gb300 import synth
+    subset = not isinstance(w.indices, np.ndarray)
+    if subset:
+        w = host_subset(w)
     indices, offsets, grad, psw = host_arrays(w)
     n_done, el, runs = 0, 0.0, 0
     wts = np.asarray(w.weights)
@@ -204,8 +236,10 @@ def cpu_baseline(w, budget_s, variant="update"):
         el += time.perf_counter() - t1
         n_done += indices.size
         runs += 1
-    return {"value": n_done / el, "unit": "lookups/s", "cores": 1, "kind": "oracle",
-            "sample": f"{runs} full step(s) of the same workload ({indices.size} lookups each), "
+    what = (f"the first {w.T} tables of the same workload" if subset else "the same workload")
+    return {"value": n_done / el, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{runs} full step(s) of {what} ({indices.size} lookups each), "
                       f"{el:.1f} s, single-threaded C++ oracle (double accumulation)"}
 
 
@@ -241,8 +275,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": DESCR[args.workload if args.workload != "large" else "dlrm"],
                                         "N": int(indices.size)},
-        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} full steps, single-threaded C++ oracle"},
+        "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(),
+                         "kind": "oracle", "sample": f"{args.steps} full steps, single-threaded C++ oracle"},
         "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -324,17 +358,21 @@ def run_forward(args):
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
+        subset = not isinstance(w.indices, np.ndarray)
+        wc = host_subset(w) if subset else w  # drawn on the device: its first two tables
+        ic, oc, _, pc = host_arrays(wc)
         n_done, el, runs = 0, 0.0, 0
         while el < min(args.cpu_seconds, 10.0):
             t1 = time.perf_counter()
-            oracle.forward(w.T, w.B, w.hash_size_cumsum, w.D_offsets, w.weights_offsets,
-                           np.asarray(w.weights), indices_h, offsets_h, per_sample_weights=psw_h,
-                           mean=(w.pooling == synth.MEAN))
+            oracle.forward(wc.T, wc.B, wc.hash_size_cumsum, wc.D_offsets, wc.weights_offsets,
+                           np.asarray(wc.weights), ic, oc, per_sample_weights=pc,
+                           mean=(wc.pooling == synth.MEAN))
             el += time.perf_counter() - t1
-            n_done += N
+            n_done += int(ic.size)
             runs += 1
-        cpu = {"value": n_done / el, "unit": "lookups/s", "cores": 1, "kind": "oracle",
-               "sample": f"{runs} full forward(s) of the same workload, {el:.1f} s, single-threaded"}
+        what = f"the first {wc.T} tables of the same workload" if subset else "the same workload"
+        cpu = {"value": n_done / el, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(),
+               "kind": "oracle", "sample": f"{runs} full forward(s) of {what}, {el:.1f} s, single-threaded"}
     print(json.dumps({
         "metric": "embedding bag forward: lookups/sec and achieved HBM GB/s vs GB300 peak",
         "op": "fwd", "value": N / (ms * 1e-3), "unit": "lookups/s", "n_gpus": 1, "steps": K,
@@ -470,7 +508,7 @@ def run_shard(args):
             el += time.perf_counter() - t1
             runs += 1
         cpu = {"value": int(recv_counts.sum()) * runs / el, "unit": "lookups/s", "cores": 1,
-               "kind": "oracle", "sample": f"{runs} step(s): rank 0's bucketize, owner {r}'s merge and "
+               "host_cores": os.cpu_count(), "kind": "oracle", "sample": f"{runs} step(s): rank 0's bucketize, owner {r}'s merge and "
                                            f"backward, {el:.1f} s, single-threaded"}
     print(json.dumps({
         "metric": "row-sharded embedding step, W ranks (exchange kernels + the most loaded owner's "
