@@ -10,12 +10,23 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/embbwd.h"
 #include "internal.cuh"
 
 using namespace embbwd;
 
 namespace {
+
+// An NVTX range over one entry point's host work: a timeline tool shows the
+// launches of the call under it. A no-op when no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls before a look-back wait gives up (~1 s)
 constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups per reduce warp slice
@@ -306,6 +317,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
                         const int64_t* momentum_offsets, emb_dtype weight_dtype,
                         emb_dtype grad_dtype, int64_t max_N, int32_t max_B,
                         int32_t max_segment_length_per_warp, uint32_t flags) {
+  NvtxRange nvtx("emb_bwd_plan");
   if (!out) return EMB_ERR_INVALID_ARG;
   *out = nullptr;
   // ---- host-side validation (no CUDA call before this point)
@@ -529,6 +541,7 @@ emb_status emb_bag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
                            const int64_t* offsets, int64_t N, int32_t B,
                            const float* per_sample_weights, const void* grad_output,
                            emb_pooling mode, float lr, void* stream) {
+  NvtxRange nvtx("emb_bag_bwd_sgd");
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
@@ -549,6 +562,7 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* moment
                                        int64_t N, int32_t B, const float* per_sample_weights,
                                        const void* grad_output, emb_pooling mode, float lr,
                                        float eps, void* stream) {
+  NvtxRange nvtx("emb_bag_bwd_rowwise_adagrad");
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
@@ -570,6 +584,7 @@ emb_status emb_bag_bwd_adagrad(emb_plan* p, void* weights, float* momentum, cons
                                const int64_t* offsets, int64_t N, int32_t B,
                                const float* per_sample_weights, const void* grad_output,
                                emb_pooling mode, float lr, float eps, void* stream) {
+  NvtxRange nvtx("emb_bag_bwd_adagrad");
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
@@ -610,6 +625,7 @@ emb_status emb_bag_bwd_dense_grad(emb_plan* p, void* grad_weights, const int64_t
                                   const int64_t* offsets, int64_t N, int32_t B,
                                   const float* per_sample_weights, const void* grad_output,
                                   emb_pooling mode, void* stream) {
+  NvtxRange nvtx("emb_bag_bwd_dense_grad");
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   const int vk = (per_sample_weights || mode == EMB_POOL_MEAN) ? VK_BAG_SCALED : VK_BAG;
   return dense_grad(p, grad_weights, indices, offsets, N, B, per_sample_weights, grad_output, vk,
@@ -619,6 +635,7 @@ emb_status emb_bag_bwd_dense_grad(emb_plan* p, void* grad_weights, const int64_t
 emb_status emb_nobag_bwd_dense_grad(emb_plan* p, void* grad_weights, const int64_t* indices,
                                     const int64_t* offsets, int64_t N, int32_t B,
                                     const void* grad_output, void* stream) {
+  NvtxRange nvtx("emb_nobag_bwd_dense_grad");
   if (p && !p->uniform_D) return EMB_ERR_INVALID_ARG;
   return dense_grad(p, grad_weights, indices, offsets, N, B, nullptr, grad_output, VK_NOBAG, 0, stream);
 }
@@ -627,6 +644,7 @@ emb_status emb_bag_fwd(emb_plan* p, const void* weights, const int64_t* indices,
                        const int64_t* offsets, int64_t N, int32_t B,
                        const float* per_sample_weights, emb_pooling mode, void* output,
                        emb_dtype output_dtype, void* stream) {
+  NvtxRange nvtx("emb_bag_fwd");
   if (!p) return EMB_ERR_INVALID_ARG;
   if (N < 0 || N > p->max_N || B <= 0 || B > p->max_B) return EMB_ERR_INVALID_ARG;
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
@@ -682,6 +700,7 @@ emb_status emb_nobag_bwd_sgd(emb_plan* p, void* weights, const int64_t* indices,
                              const int64_t* offsets, int64_t N, int32_t B,
                              const void* grad_output, float lr, emb_nobag_path path,
                              void* stream) {
+  NvtxRange nvtx("emb_nobag_bwd_sgd");
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (!p->uniform_D) return EMB_ERR_INVALID_ARG;
   if (path < EMB_NOBAG_AUTO || path > EMB_NOBAG_ATOMIC) return EMB_ERR_INVALID_ARG;

@@ -18,6 +18,8 @@
 //
 // No kernel here waits on another block: scans are three-phase (block sums, one
 // block over the sums, block rescans), so nothing can stall.
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <vector>
 
@@ -545,6 +547,8 @@ emb_status emb_shard_bucketize(emb_shard* sh, const int64_t* indices, const int6
                                int64_t N, int32_t B, const float* per_sample_weights,
                                emb_pooling mode, int64_t* send_offsets, int64_t* send_indices,
                                float* send_scales, int64_t* send_counts, void* stream) {
+  nvtxRangePushA("emb_shard_bucketize");
+  struct Pop { ~Pop() { nvtxRangePop(); } } pop;
   if (!sh || !offsets || !send_offsets || !send_counts) return EMB_ERR_INVALID_ARG;
   if (B <= 0 || B > sh->max_B || N < 0 || N >= (1ll << 31)) return EMB_ERR_INVALID_ARG;
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
@@ -620,6 +624,8 @@ emb_status emb_shard_merge(emb_shard* sh, const int64_t* recv_offsets, const int
                            const float* recv_scales, int64_t n_recv, int32_t B,
                            int64_t* merged_offsets, int64_t* merged_indices, float* merged_scales,
                            void* stream) {
+  nvtxRangePushA("emb_shard_merge");
+  struct Pop { ~Pop() { nvtxRangePop(); } } pop;
   if (!sh || !recv_offsets || !merged_offsets) return EMB_ERR_INVALID_ARG;
   if (B <= 0 || B > sh->max_B || n_recv < 0 || n_recv >= (1ll << 31)) return EMB_ERR_INVALID_ARG;
   if (n_recv > 0 && (!recv_indices || !merged_indices)) return EMB_ERR_INVALID_ARG;
