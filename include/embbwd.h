@@ -17,8 +17,16 @@
  *   ("tt_embeddings_cuda.cu": update_tt_cores_sgd_kernel and
  *    cache_backward_rowwise_adagrad_approx_kernel give the two update rules;
  *    here they act on the de-duplicated row gradient.)
- *   The update is computed in fp32 and rounded once (round-to-nearest-even)
- *   to the weight's storage type. Rows that no lookup touches are not written.
+ *   The update is computed in fp32 and rounded once (round-to-nearest-even,
+ *   or stochastically with EMB_FLAG_STOCHASTIC_ROUNDING) to the weight's
+ *   storage type. Rows that no lookup touches are not written.
+ *
+ * Also declared here: elementwise Adagrad (emb_bag_bwd_adagrad), the
+ * dense-gradient mode (emb_bag_bwd_dense_grad, emb_nobag_bwd_dense_grad), the
+ * forward pooled lookup (emb_bag_fwd), an allocation-free unpooled update
+ * (emb_nobag_bwd_sgd_atomic_noalloc), and the exchange step of row-sharded
+ * tables over several ranks (emb_shard_*). emb_shard_bucketize is the one call
+ * that synchronises (it returns the exchange's split sizes).
  *
  * Layouts (all element offsets, not bytes):
  *   weights        flat; row idx of table t starts at weights_offsets[t] + idx*D_t
