@@ -5,9 +5,12 @@
 
 One step = one whole pass of the hot path (linearise, sort, run-length encode,
 long-run partition, fused reduce + optimizer) over one synthetic batch. The
-default workload is the DLRM-like one (8 tables x 100k rows, D=64 fp32, B=2048,
-bag length U{1..20}, Zipf(1.05) ids, row-wise Adagrad). Its working set is far
-below L2, so a 256 MB buffer is written between timed steps to flush L2.
+default workload is the large skewed one, the largest that fits one GPU (64
+tables x 2M rows, D=128 fp16 weights + fp32 row-wise state, B=65536, bag length
+power law on [1, 500] with mean 30, Zipf(1.2) ids, ~1.26e8 lookups, drawn on the
+device). Its inputs (37 GB) are far larger than L2; a 256 MB buffer is still
+written between timed steps, as for the small workloads, whose working sets fit
+in L2.
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own batch on
 its own GPU (weak scaling, no collective: tables are independent).
@@ -40,9 +43,9 @@ DESCR = {
              "Zipf(1.2) ids, sum, row-wise Adagrad",
 }
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# dominant kernel, from the ncu captures summarised under profiles/; a workload
-# without an entry for the current kernels reports null.
-TRAFFIC = {("dlrm", "reduce_update"): 21_136_640}  # profiles/k_reduce_dlrm.md
+# dominant kernel, from ncu captures of the current kernels; a workload without
+# an entry reports null.
+TRAFFIC = {("dlrm", "reduce_update"): 21_136_640}
 
 
 def parse():
@@ -51,7 +54,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dlrm", choices=list(DESCR))
+    ap.add_argument("--workload", default="large", choices=list(DESCR))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="plain launches instead of programmatic dependent launches")
@@ -64,15 +67,18 @@ def parse():
                     help="bwd: update = the workload's optimizer; dense = dense-gradient mode; "
                          "adagrad = elementwise Adagrad; sr = the update with stochastic rounding")
     ap.add_argument("--shards", type=int, default=8, help="ranks W of --op shard")
+    ap.add_argument("--tables", type=int, default=None,
+                    help="large workload only: draw just its first K tables (a cut-down case of the "
+                         "same kernels, e.g. for profiler captures)")
     ap.add_argument("--shard-map", default="cyclic", choices=["cyclic", "ranges"],
                     help="row map of --op shard: rows modulo W, or contiguous ranges")
     return ap.parse_args()
 
 
-def make_workload(name, seed, device):
+def make_workload(name, seed, device, tables=None):
     from sparse_embedding_bag_gb300 import synth
     if name == "large":
-        return synth.large_on_device(seed, device=device)
+        return synth.large_on_device(seed, device=device, tables=tables)
     return synth.BY_NAME[name](seed)
 
 
@@ -83,31 +89,41 @@ def host_arrays(w):
     return conv(w.indices), conv(w.offsets), conv(w.grad_output), conv(w.per_sample_weights)
 
 
-def algorithmic_bytes(w, indices, offsets, variant="update"):
+def algorithmic_bytes(w, variant="update"):
     """Minimal bytes of one step: int64 indices, the gradient row read per lookup,
     and one read + one write of every unique row (and its fp32 state for Adagrad:
     8 bytes per row row-wise, 8 per element elementwise). The dense-gradient mode
     writes every unique row once and clears the whole weights-sized buffer.
-    Returns (step bytes, reduce-kernel bytes, unique rows)."""
+    Counted with torch on the device that holds the workload's arrays (host numpy
+    arrays are counted on the CPU). Returns (step bytes, reduce-kernel bytes,
+    unique rows)."""
+    import torch
     from sparse_embedding_bag_gb300 import synth
-    lengths = np.diff(offsets)
-    t_of_lookup = np.repeat(np.arange(w.T * w.B) // w.B, lengths)
-    keys = w.hash_size_cumsum[t_of_lookup] + indices
-    uniq = np.unique(keys)
-    t_of_row = np.searchsorted(w.hash_size_cumsum, uniq, side="right") - 1
+    on_dev = isinstance(w.indices, torch.Tensor)
+    dev = w.indices.device if on_dev else torch.device("cpu")
+    idx = torch.as_tensor(w.indices, device=dev)
+    off = torch.as_tensor(w.offsets, device=dev)
+    hsc = torch.as_tensor(np.asarray(w.hash_size_cumsum, np.int64), device=dev)
+    dims = torch.as_tensor(np.asarray(w.dims, np.int64), device=dev)
+    t_of_lookup = torch.repeat_interleave(torch.arange(w.T * w.B, device=dev) // w.B, off[1:] - off[:-1])
+    uniq = torch.unique(hsc[t_of_lookup] + idx)
+    t_of_row = torch.searchsorted(hsc, uniq, right=True) - 1
     gsize = 4 if w.grad_dtype == synth.F32 else 2
     wsize = 4 if w.weight_dtype == synth.F32 else 2
-    grad_bytes = int(w.dims[t_of_lookup].astype(np.int64).sum()) * gsize
-    row_elems = int(w.dims[t_of_row].astype(np.int64).sum())
+    grad_bytes = int(dims[t_of_lookup].sum()) * gsize
+    row_elems = int(dims[t_of_row].sum())
+    n_uniq, N = int(uniq.numel()), int(idx.numel())
+    del t_of_lookup, uniq, t_of_row
     row_bytes = row_elems * 2 * wsize
-    state = 8 * uniq.size if w.optimizer == synth.ROWWISE_ADAGRAD else 0
+    state = 8 * n_uniq if w.optimizer == synth.ROWWISE_ADAGRAD else 0
     if variant == "adagrad":
         state = 8 * row_elems
     if variant == "dense":
         reduce_bytes = grad_bytes + row_elems * wsize
-        return 8 * indices.size + reduce_bytes + int(np.asarray(w.weights).size) * wsize, reduce_bytes, int(uniq.size)
+        return 8 * N + reduce_bytes + int(w.weights.numel() if on_dev else np.asarray(w.weights).size) * wsize, \
+            reduce_bytes, n_uniq
     reduce_bytes = grad_bytes + row_bytes + state
-    return 8 * indices.size + reduce_bytes, reduce_bytes, int(uniq.size)
+    return 8 * N + reduce_bytes, reduce_bytes, n_uniq
 
 
 class ClockSampler:
@@ -175,7 +191,7 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def host_subset(w, tables=2):
+def host_subset(w, tables=1):
     """A workload drawn on the device, cut to its first `tables` tables on the host
     (tables are independent, so the oracle's rate per lookup carries over)."""
     import dataclasses
@@ -205,10 +221,11 @@ def torch_int16():
 
 def cpu_baseline(w, budget_s, variant="update"):
     """The oracle, as it stands (single thread), on the same workload for ~budget_s seconds
-    (for a workload drawn on the device, on its first two tables)."""
+    (for a workload drawn on the device, on its first table)."""
     import oracle
     from sparse_embedding_bag_gb300 import synth
     subset = not isinstance(w.indices, np.ndarray)
+    w_full_T = w.T
     if subset:
         w = host_subset(w)
     indices, offsets, grad, psw = host_arrays(w)
@@ -236,7 +253,7 @@ def cpu_baseline(w, budget_s, variant="update"):
         el += time.perf_counter() - t1
         n_done += indices.size
         runs += 1
-    what = (f"the first {w.T} tables of the same workload" if subset else "the same workload")
+    what = (f"the first {w.T} of the {w_full_T} tables of the same workload" if subset else "the same workload")
     return {"value": n_done / el, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{runs} full step(s) of {what} ({indices.size} lookups each), "
@@ -244,14 +261,26 @@ def cpu_baseline(w, budget_s, variant="update"):
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle timed on the same workload, metric and unit."""
+    """Reference arm: the CPU oracle timed on the same workload, metric and unit.
+    The large workload (32.8 GB of weights) is timed on its first table, drawn on
+    the device when there is one, so that it is exactly the first table of the
+    workload the GPU arm times (tables are independent: the rate per lookup
+    carries over); one step of it is a few seconds of one host core."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
     from sparse_embedding_bag_gb300 import synth
     oracle.build()
-    w = make_workload(args.workload if args.workload != "large" else "dlrm", 0, "cpu")
+    if args.workload == "large":
+        import torch
+        gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+        w = host_subset(make_workload("large", 0, gen_dev, tables=1), tables=1)
+        sample = (f"table 1 of the 64 tables of the same workload ({w.N} lookups per step)" +
+                  ("" if gen_dev == "cuda" else ", drawn with the CPU generator (same recipe, other draws)"))
+    else:
+        w = make_workload(args.workload, 0, "cpu")
+        sample = f"the whole workload ({w.N} lookups per step)"
     indices, offsets, grad, psw = host_arrays(w)
 
     def one():
@@ -273,10 +302,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "lookups/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": DESCR[args.workload if args.workload != "large" else "dlrm"],
-                                        "N": int(indices.size)},
+        "data": "synthetic", "config": {"workload": DESCR[args.workload], "N": int(indices.size)},
         "cpu_baseline": {"value": value, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(),
-                         "kind": "oracle", "sample": f"{args.steps} full steps, single-threaded C++ oracle"},
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps of {sample}, single-threaded C++ oracle "
+                                   f"(double accumulation)"},
         "e2e": {"value": value, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -359,7 +389,7 @@ def run_forward(args):
     if not args.no_cpu_baseline:
         import oracle
         subset = not isinstance(w.indices, np.ndarray)
-        wc = host_subset(w) if subset else w  # drawn on the device: its first two tables
+        wc = host_subset(w) if subset else w  # drawn on the device: its first table
         ic, oc, _, pc = host_arrays(wc)
         n_done, el, runs = 0, 0.0, 0
         while el < min(args.cpu_seconds, 10.0):
@@ -559,14 +589,14 @@ def main():
     b.build()
     E.load()
 
-    w = make_workload(args.workload, rank, f"cuda:{local}")
+    w = make_workload(args.workload, rank, f"cuda:{local}", tables=args.tables)
     variant = args.variant
     if variant == "sr" and w.weight_dtype == synth.F32:
         raise SystemExit("--variant sr needs a workload with fp16 / bf16 weights (mixed, large)")
     if variant == "adagrad" and w.nobag:
         raise SystemExit("--variant adagrad needs a pooled workload")
     indices_h, offsets_h, grad_h, psw_h = host_arrays(w)
-    step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, indices_h, offsets_h, variant)
+    step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, variant)
     dw = dev.to_device(w, f"cuda:{local}")
     flags = (E.EMB_FLAG_NO_PDL if args.no_pdl else 0) | (E.EMB_FLAG_STOCHASTIC_ROUNDING if variant == "sr" else 0)
     plan = dev.make_plan(w, device_index=local, flags=flags)
@@ -689,6 +719,10 @@ def main():
     }
     dom_name = names[dom]
     achieved = stage_bytes.get(dom_name, 0) / launches[dom] / (per_launch[dom] * 1e-3) / 1e9
+    # measured DRAM bytes of one launch of the dominant kernel (null without a capture
+    # of the current kernels on this workload); its rate over the event-timed launch
+    traffic = TRAFFIC.get((args.workload, dom_name)) if (args.tables is None and variant == "update") else None
+    dram_gbs = traffic / (per_launch[dom] * 1e-3) / 1e9 if traffic else None
     red_achieved = reduce_bytes / (stage[4] * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers (H2D + call + status read)
@@ -732,7 +766,8 @@ def main():
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.workload], "N": n_local, "unique_rows": uniq,
+        "config": {"workload": DESCR[args.workload] + (f" (first {w.T} tables only)" if args.tables else ""),
+                   "N": n_local, "unique_rows": uniq,
                    "variant": {"update": "the workload's optimizer", "dense": "dense-gradient mode",
                                "adagrad": "elementwise Adagrad",
                                "sr": "the workload's optimizer, stochastic rounding"}[variant],
@@ -742,7 +777,8 @@ def main():
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": TRAFFIC.get((args.workload, dom_name))},
+                     "traffic": traffic, "dram_gbs": dram_gbs,
+                     "dram_frac": None if dram_gbs is None else dram_gbs / peak},
         "reduce_update": {"ms": float(stage[4]), "gbs": red_achieved, "frac": red_achieved / peak,
                           "bytes": reduce_bytes},
         "stage_ms": {n: float(v) for n, v in zip(names, stage) if n != "-"},

@@ -231,12 +231,18 @@ def lm(seed: int = 0, tokens: int = 8 * 4096, vocab: int = 128256, D: int = 4096
 LARGE = dict(T=64, E=2_000_000, D=128, B=65536, kmax=500, mean_len=30.0, zipf_a=1.2)
 
 
-def large_on_device(seed: int = 0, device="cuda", T=None, B=None, E=None):
+def large_on_device(seed: int = 0, device="cuda", T=None, B=None, E=None, tables=None):
     """The large skewed workload, drawn on the device (too big for host-side numpy).
 
     Returns a Workload whose arrays are torch tensors on `device`. Bag lengths
     follow P(k) ~ k^-a on 1..500 with a chosen so the mean is 30; ids are
     bounded Zipf(1.2) per table (rank k -> row k-1).
+
+    Every table draws from its own generator (seeded seed * 2^16 + t): its bag
+    lengths, its ids, its weights and its [B, D] column block of grad_output.
+    `tables` = k draws only the first k tables, which are then exactly the
+    first k tables of the full workload (tables are independent, so that cut is
+    a workload of its own with the same per-table statistics).
     """
     import torch
     p = dict(LARGE)
@@ -244,35 +250,44 @@ def large_on_device(seed: int = 0, device="cuda", T=None, B=None, E=None):
     B = p["B"] if B is None else B
     E = p["E"] if E is None else E
     D = p["D"]
-    gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
+    T_draw = T if tables is None else min(int(tables), T)
+    gens = []
+    for t in range(T_draw):
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 65536 + t)
+        gens.append(g)
     a_len = power_law_exponent_for_mean(p["mean_len"], p["kmax"])
     k = torch.arange(1, p["kmax"] + 1, dtype=torch.float64, device=device)
     len_cdf = torch.cumsum(k ** (-a_len), 0)
     len_cdf /= len_cdf[-1].clone()
-    u = torch.rand(T * B, generator=gen, device=device, dtype=torch.float64)
-    lengths = torch.searchsorted(len_cdf, u, right=True).clamp_(max=p["kmax"] - 1) + 1
-    offsets = torch.zeros(T * B + 1, dtype=torch.int64, device=device)
+    lengths = torch.empty(T_draw * B, dtype=torch.int64, device=device)
+    for t in range(T_draw):
+        u = torch.rand(B, generator=gens[t], device=device, dtype=torch.float64)
+        lengths[t * B:(t + 1) * B] = torch.searchsorted(len_cdf, u, right=True).clamp_(max=p["kmax"] - 1) + 1
+    offsets = torch.zeros(T_draw * B + 1, dtype=torch.int64, device=device)
     offsets[1:] = torch.cumsum(lengths, 0)
     N = int(offsets[-1].item())
     kk = torch.arange(1, E + 1, dtype=torch.float64, device=device)
     id_cdf = torch.cumsum(kk ** (-p["zipf_a"]), 0)
     id_cdf /= id_cdf[-1].clone()
     indices = torch.empty(N, dtype=torch.int64, device=device)
-    chunk = 1 << 24
-    for s in range(0, N, chunk):
-        e = min(N, s + chunk)
-        uu = torch.rand(e - s, generator=gen, device=device, dtype=torch.float64)
-        indices[s:e] = torch.searchsorted(id_cdf, uu, right=True).clamp_(max=E - 1)
-    rows = np.full(T, E, np.int64)
-    dims = np.full(T, D, np.int32)
+    bounds = offsets[::B].cpu().numpy()
+    for t in range(T_draw):
+        a, b = int(bounds[t]), int(bounds[t + 1])
+        uu = torch.rand(b - a, generator=gens[t], device=device, dtype=torch.float64)
+        indices[a:b] = torch.searchsorted(id_cdf, uu, right=True).clamp_(max=E - 1)
+    rows = np.full(T_draw, E, np.int64)
+    dims = np.full(T_draw, D, np.int32)
     hsc, Do, wo = table_layout(rows, dims)
-    weights = torch.empty(T * E * D, dtype=torch.float16, device=device)
-    for s in range(0, weights.numel(), 1 << 28):
-        e = min(weights.numel(), s + (1 << 28))
-        weights[s:e] = (torch.rand(e - s, generator=gen, device=device) * 0.2 - 0.1).to(torch.float16)
-    momentum = torch.zeros(T * E, dtype=torch.float32, device=device)
-    grad = torch.randn(B, T * D, generator=gen, device=device, dtype=torch.float32)
+    weights = torch.empty(T_draw * E * D, dtype=torch.float16, device=device)
+    for t in range(T_draw):
+        s = t * E * D
+        weights[s:s + E * D] = (torch.rand(E * D, generator=gens[t], device=device) * 0.2 - 0.1).to(torch.float16)
+    momentum = torch.zeros(T_draw * E, dtype=torch.float32, device=device)
+    grad = torch.empty(B, T_draw * D, device=device, dtype=torch.float32)
+    for t in range(T_draw):
+        grad[:, t * D:(t + 1) * D] = torch.randn(B, D, generator=gens[t], device=device, dtype=torch.float32)
+    T = T_draw
     return Workload(name="large", T=T, B=B, rows=rows, dims=dims, hash_size_cumsum=hsc,
                     D_offsets=Do, weights_offsets=wo, momentum_offsets=None, weight_dtype=F16,
                     grad_dtype=F32, optimizer=ROWWISE_ADAGRAD, pooling=SUM, nobag=False,
