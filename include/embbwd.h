@@ -234,10 +234,13 @@ emb_status emb_bag_fwd(emb_plan* plan, const void* weights, const int64_t* indic
  *   until the process exits. Limits: N <= 4194304 lookups, T <= 4096 tables,
  *   B*T < 2^31, D a multiple of 4 and <= 4096; beyond them EMB_ERR_INVALID_ARG.
  *   hash_size_cumsum (int64[T+1]) and weights_offsets (int64[T]) are caller-owned
- *   DEVICE arrays here; weights are fp32; grad_output is [N, D] of grad_dtype.
- *   device_status (device uint32, may be NULL) receives this call's device error
- *   bits: 1 = an index outside its table, 2 = malformed offsets or
- *   hash_size_cumsum; 0 = none. Nothing is updated when a bit is set.
+ *   DEVICE arrays here, checked on the device before any update: hash_size_cumsum
+ *   starts at 0, strictly increases and stays below 2^32; every weights_offsets[t]
+ *   is >= 0 and a multiple of 4. weights are fp32; grad_output is [N, D] of
+ *   grad_dtype. device_status (device uint32, may be NULL) receives this call's
+ *   device error bits: 1 = an index outside its table, 2 = malformed offsets,
+ *   hash_size_cumsum or weights_offsets; 0 = none. Nothing is updated when a bit
+ *   is set.
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   All calls share the scratch array: calls that overlap on the GPU race, so

@@ -58,12 +58,21 @@ cudaError_t scratch_address(int device, NoAllocScratch** out) {
 }
 
 // hash_size_cumsum (int64, device) -> 32-bit copy in the scratch, with the
-// checks emb_bwd_plan does on the host: starts at 0, strictly increasing, < 2^32.
-__global__ void k_tables32(const int64_t* __restrict__ hsc, uint32_t T, NoAllocScratch* s) {
+// checks emb_bwd_plan does on the host: hash_size_cumsum starts at 0, is
+// strictly increasing and < 2^32; every weights_offsets[t] is >= 0 and a
+// multiple of 4 (the atomic scatter adds 16-byte vectors at
+// weights + weights_offsets[t] + idx * D). A failed check sets kErrOffsets,
+// after which the scatter kernel returns before touching the weights.
+__global__ void k_tables32(const int64_t* __restrict__ hsc, const int64_t* __restrict__ wo, uint32_t T,
+                           NoAllocScratch* s) {
   for (uint32_t t = threadIdx.x; t <= T; t += blockDim.x) {
     const int64_t v = hsc[t];
     bool bad = v < 0 || v > (int64_t)0xffffffffLL || (t == 0 && v != 0);
     if (t > 0) bad |= v <= hsc[t - 1];
+    if (t < T) {
+      const int64_t o = wo[t];
+      bad |= o < 0 || (o & 3) != 0;
+    }
     if (bad) {
       atomicOr(&s->ctl.err, kErrOffsets);
       atomicOr(&s->status, kErrOffsets);
@@ -103,7 +112,7 @@ extern "C" emb_status emb_nobag_bwd_sgd_atomic_noalloc(
   cudaError_t e = scratch_address(device, &sc);
   if (e == cudaSuccess) e = cudaMemsetAsync(sc, 0, offsetof(NoAllocScratch, hsc), s);
   if (e == cudaSuccess && N > 0) {
-    k_tables32<<<1, kThreads, 0, s>>>(hash_size_cumsum, (uint32_t)T, sc);
+    k_tables32<<<1, kThreads, 0, s>>>(hash_size_cumsum, weights_offsets, (uint32_t)T, sc);
     e = cudaGetLastError();
     DecodeArgs d;
     d.indices = indices;

@@ -7,13 +7,17 @@ fixed static device array. This file is collected last so that a run stopping
 at its first failure has already run every other test.
 
 Checked through the C ABI against the existing entry point (a plan plus
-emb_nobag_bwd_sgd with the atomic path), within the parity tolerance, on two
-calls in a row each, so that the shared scratch being left over from the
-previous call is exercised.
+emb_nobag_bwd_sgd with the atomic path) and against the CPU oracle's unpooled
+SGD step, within the parity tolerance, on two calls in a row each, so that the
+shared scratch being left over from the previous call is exercised. Malformed
+device-side table arrays (a misaligned or negative weights offset, a
+hash_size_cumsum that does not increase) must be reported in device_status with
+nothing updated, and the next valid call must start clean.
 """
 import numpy as np
 import pytest
 
+from _helpers import oracle_step
 from sparse_embedding_bag_gb300 import device as dev
 from sparse_embedding_bag_gb300 import embbwd as E
 from sparse_embedding_bag_gb300 import synth
@@ -40,7 +44,7 @@ def _workload(seed, grad_dtype=synth.F32):
         lambda r, t, n: synth.sample_zipf(r, rows[t], 1.1, n), nobag=True, grad_dtype=grad_dtype)
 
 
-@pytest.mark.parametrize("grad_dtype", [synth.F32, synth.BF16])
+@pytest.mark.parametrize("grad_dtype", [synth.F32, synth.F16, synth.BF16])
 def test_noalloc_matches_planned_atomic_path_twice(grad_dtype):
     import torch
     w = _workload(11, grad_dtype)
@@ -65,6 +69,22 @@ def test_noalloc_matches_planned_atomic_path_twice(grad_dtype):
     finally:
         E.emb_plan_destroy(plan)
     assert not np.array_equal(new.weights.cpu().numpy(), w.weights)  # it did update
+
+
+@pytest.mark.parametrize("grad_dtype", [synth.F32, synth.F16])
+def test_noalloc_matches_oracle(grad_dtype):
+    import torch
+    w = _workload(13, grad_dtype)
+    d = dev.to_device(w)
+    hsc = torch.from_numpy(w.hash_size_cumsum).cuda()
+    wo = torch.from_numpy(w.weights_offsets).cuda()
+    status = torch.full((1,), 0xFFFF, dtype=torch.int32, device="cuda")
+    E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, int(w.dims[0]), d.weights, d.indices,
+                                       d.offsets, w.N, w.B, d.grad_output, w.grad_dtype, w.lr, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    exp, _ = oracle_step(w)
+    np.testing.assert_allclose(d.weights.cpu().numpy(), exp, rtol=RTOL, atol=ATOL)
 
 
 def test_noalloc_reports_errors_and_limits():
@@ -93,6 +113,39 @@ def test_noalloc_reports_errors_and_limits():
     # the next valid call starts clean
     E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, hsc, wo, D, d.weights, d.indices, d.offsets, w.N,
                                        w.B, d.grad_output, w.grad_dtype, w.lr, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert not torch.equal(d.weights, before)
+
+
+@pytest.mark.parametrize("case", ["misaligned_offset", "negative_offset", "flat_cumsum"])
+def test_noalloc_rejects_malformed_tables_on_device(case):
+    """The device-side table arrays are checked before the scatter runs: a bad one
+    sets bit 2 of device_status and leaves the weights untouched; the next valid
+    call succeeds."""
+    import torch
+    w = _workload(14)
+    d = dev.to_device(w)
+    hsc_h, wo_h = w.hash_size_cumsum.copy(), w.weights_offsets.copy()
+    if case == "misaligned_offset":
+        wo_h[1] += 2
+    elif case == "negative_offset":
+        wo_h[2] = -4
+    else:
+        hsc_h[2] = hsc_h[1]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    D = int(w.dims[0])
+    before = d.weights.clone()
+    E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, torch.from_numpy(hsc_h).cuda(), torch.from_numpy(wo_h).cuda(),
+                                       D, d.weights, d.indices, d.offsets, w.N, w.B, d.grad_output,
+                                       w.grad_dtype, w.lr, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    assert torch.equal(d.weights, before)
+    E.emb_nobag_bwd_sgd_atomic_noalloc(0, w.T, torch.from_numpy(w.hash_size_cumsum).cuda(),
+                                       torch.from_numpy(w.weights_offsets).cuda(), D, d.weights,
+                                       d.indices, d.offsets, w.N, w.B, d.grad_output, w.grad_dtype,
+                                       w.lr, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert not torch.equal(d.weights, before)
