@@ -102,9 +102,10 @@ struct emb_plan {
   uint32_t seq = 0;
   int reduce_grid[3][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}};  // [optimizer][value kind]
   int64_t w_extent = 0;  // elements of the weights layout: max over t of offset + rows * D
-  // Blocks that fit on the GPU at once: sort pass [tile class][wide payload], k_runs [split].
+  // Blocks that fit on the GPU at once: sort pass [tile class][wide payload], k_runs
+  // [split][8 or 16 keys per thread].
   int pass_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};  // [pass tile class][wide values]
-  int runs_cap[2] = {0, 0};
+  int runs_cap[2][2] = {{0, 0}, {0, 0}};
   int fwd_grid[3] = {0, 0, 0};  // forward kernel grid per output type (0: not set up yet)
   cudaStream_t last_stream = nullptr;
   int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
@@ -235,14 +236,15 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.run_key = p->run_key;
   ra.run_start = p->run_start;
   ra.thr = p->thr;
-  ra.ordered = (N + kRleTile - 1) / kRleTile <= p->runs_cap[si];
+  const int items = runs_items_for(N);
+  ra.ordered = (N + (int64_t)kThreads * items - 1) / ((int64_t)kThreads * items) <= p->runs_cap[si][items == 16];
   ra.long_ids = p->long_ids;
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
   ra.seg_keys = p->split[si].d_segkeys;
   ra.S = (uint32_t)p->split[si].segs.size() - 1;
   ra.seg_runs = p->seg_runs;
-  EMB_CUDA(launch_runs(ra, s, pdl));
+  EMB_CUDA(launch_runs(ra, items, s, pdl));
   EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel (no event 4)
 
   ReduceArgs r;
@@ -508,13 +510,15 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       e = cudaMemcpy(sp.d_segkeys, keys.data(), keys.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = sort_configure(p->props);
+  if (e == cudaSuccess) e = runs_configure();
   if (e == cudaSuccess) {
     const int tiles[3] = {kThreads * 4, kThreads * 8, kThreads * 16};
     for (int c = 0; c < 3; ++c)
       for (int wide = 0; wide < 2; ++wide)
         p->pass_cap[c][wide] = sort_pass_capacity(wide != 0, tiles[c], p->props.sms);
     for (int opt = 0; opt < 2; ++opt)
-      p->runs_cap[opt] = runs_capacity((int)p->split[opt].segs.size() - 1, p->props.sms);
+      for (int it = 0; it < 2; ++it)
+        p->runs_cap[opt][it] = runs_capacity((int)p->split[opt].segs.size() - 1, it ? 16 : 8, p->props.sms);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

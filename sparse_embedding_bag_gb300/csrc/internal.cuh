@@ -33,8 +33,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kMaxPasses = 4;  // 32-bit keys
-constexpr int kRleItems = 8;
-constexpr int kRleTile = kThreads * kRleItems;
+constexpr int kRleItems = 8;   // sorted keys per thread of k_runs (16 for large batches)
+constexpr int kRleTile = kThreads * kRleItems;  // smallest k_runs tile
 constexpr int kMaxT = 4096;
 
 // Device-side error bits (per call in Ctl::err, accumulated in the plan's sticky word).
@@ -572,11 +572,13 @@ cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s
 cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl);
 // Blocks of the pass kernel (and of k_runs) that fit on the GPU at once.
 int sort_pass_capacity(bool wide_vals, int tile, int sms);
-int runs_capacity(int S, int sms);
+int runs_capacity(int S, int items, int sms);
 cudaError_t sort_configure(const DevProps& p);
 
-// runs.cu
-cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl);
+// runs.cu: items = sorted keys per thread (8 or 16, runs_items_for(N)).
+int runs_items_for(int64_t N);
+cudaError_t launch_runs(const RunsArgs& a, int items, cudaStream_t s, bool pdl);
+cudaError_t runs_configure();
 
 // forward.cu: forward pooled lookup kernel of (weight type, output type, kv), or nullptr.
 const void* fwd_kernel(int weight_dtype, int out_dtype, int kv);

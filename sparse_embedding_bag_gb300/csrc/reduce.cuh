@@ -177,10 +177,12 @@ __device__ __forceinline__ void team_gather(const ReduceArgs& a, const RowShape&
 }
 
 // Adds up the groups of a team (xor over lane offsets Lg .. Lt/2): afterwards
-// every group of the team holds the run's totals. Shuffles are warp-uniform.
+// every group of the team holds the run's totals. Shuffles are warp-uniform:
+// they start at lane offset Lg0, the smallest group width of the warp's teams
+// (teams whose groups are wider skip the offsets below their width).
 template <int KV>
-__device__ __forceinline__ void team_fold(float4 (&acc)[KV], uint32_t Lg, uint32_t Lt) {
-  for (uint32_t off = 1; off < Lt; off <<= 1) {
+__device__ __forceinline__ void team_fold(float4 (&acc)[KV], uint32_t Lg, uint32_t Lt, uint32_t Lg0) {
+  for (uint32_t off = Lg0; off < Lt; off <<= 1) {
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       float4 y;
@@ -388,7 +390,7 @@ __device__ __forceinline__ void sum_pieces(const ReduceArgs& a, const RowShape& 
 #pragma unroll
       for (int kv = 0; kv < KV; ++kv) acc[kv] = f4_add(x[u][kv], acc[kv]);
   }
-  team_fold<KV>(acc, 1u << rs.lg, 32);
+  team_fold<KV>(acc, 1u << rs.lg, 32, 1u << rs.lg);
 }
 
 // Arrival of one piece (acc: its sum in every lane group). Returns true in the
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
         const uint32_t steps = (je - jb + Pg * UNR - 1) / (Pg * UNR);
         float4 acc[KV];
         team_gather<VK, grad_t, KV, PrefetchVals<VK, MULTI>::value>(a, rs, jb, je, steps, Pg, g, li, acc);
-        team_fold<KV>(acc, 1u << rs.lg, 32);
+        team_fold<KV>(acc, 1u << rs.lg, 32, 1u << rs.lg);
         if (whole) {  // long runs: the row is read after the gather (registers)
           load_row<emb_t, OPT, KV>(a, rs, true, g, li, wv);
           if constexpr (OPT == 1) m_old = a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx];
@@ -570,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
     const uint32_t steps = __reduce_max_sync(0xffffffffu, my_steps);
     float4 acc[KV];
     team_gather<VK, grad_t, KV, PrefetchVals<VK, MULTI>::value>(a, rs, start, end, steps, Pt, g, li, acc);
-    team_fold<KV>(acc, 1u << rs.lg, Lt);
+    const uint32_t lg0 = __reduce_min_sync(0xffffffffu, active ? rs.lg : 5u);
+    team_fold<KV>(acc, 1u << rs.lg, Lt, 1u << lg0);
     update_row<emb_t, OPT, KV>(a, rs, active, g, li, tl, Lt, acc, wv, m_old);
   };
   if constexpr (!MULTI) {  // one team shape for all tables: one sweep over all runs

@@ -10,7 +10,7 @@
 //     append, each with its place in the concatenation of all long runs (the
 //     prefix sum of their lengths), which the reduce cuts into equal slices.
 //
-// Each block owns a tile of kRleTile sorted keys and the runs whose first
+// Each block owns a tile of 256 * ITEMS sorted keys and the runs whose first
 // lookup lies in it. A run that continues past the tile end has its end found
 // by a 32-lane parallel upper-bound search (a few rounds of one load per lane),
 // so every run's length is known inside the block that owns it. When the tables
@@ -53,16 +53,24 @@ __device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ 
   return (uint32_t)lo;
 }
 
+// Dynamic shared memory: run-head positions [TILE+1], first keys of segments [S+1].
+template <int ITEMS>
+size_t runs_smem(uint32_t S) {
+  return ((size_t)kThreads * ITEMS + 1 + S + 1) * sizeof(uint32_t);
+}
+
 // MULTI: the tables form several segments whose first runs are recorded.
-template <bool MULTI>
+template <bool MULTI, int ITEMS>
 __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
+  constexpr uint32_t TILE = kThreads * ITEMS;
   __shared__ uint32_t s_tile;
-  __shared__ uint32_t s_scan[2 * kWarps];
+  __shared__ uint32_t s_scan[3 * kWarps];
   __shared__ uint32_t s_base[3];
   __shared__ uint32_t s_last_key;
   __shared__ uint32_t s_end_key;  // key at position N-1 (last tile only)
-  __shared__ uint32_t s_head_pos[kRleTile + 1];
-  extern __shared__ uint32_t s_bkey[];  // [S+1] first key of each segment
+  extern __shared__ __align__(16) uint32_t s_dyn[];
+  uint32_t* s_head_pos = s_dyn;            // [TILE+1]
+  uint32_t* s_bkey = s_head_pos + TILE + 1;  // [S+1]
   if constexpr (MULTI)
     for (uint32_t i = threadIdx.x; i <= a.S; i += kThreads) s_bkey[i] = a.seg_keys[i];
   pdl_wait();
@@ -76,24 +84,25 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
     return;
   }
   const uint32_t N = (uint32_t)a.N;
-  const uint32_t i0 = tile * kRleTile;
-  const uint32_t p0 = i0 + threadIdx.x * kRleItems;
+  const uint32_t i0 = tile * TILE;
+  const uint32_t p0 = i0 + threadIdx.x * ITEMS;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  uint32_t key[kRleItems];
-  if (p0 + kRleItems <= N) {
-    const uint4 u0 = *reinterpret_cast<const uint4*>(a.keys + p0);
-    const uint4 u1 = *reinterpret_cast<const uint4*>(a.keys + p0 + 4);
-    key[0] = u0.x; key[1] = u0.y; key[2] = u0.z; key[3] = u0.w;
-    key[4] = u1.x; key[5] = u1.y; key[6] = u1.z; key[7] = u1.w;
+  uint32_t key[ITEMS];
+  if (p0 + ITEMS <= N) {
+#pragma unroll
+    for (int k = 0; k < ITEMS; k += 4) {
+      const uint4 u = *reinterpret_cast<const uint4*>(a.keys + p0 + k);
+      key[k] = u.x; key[k + 1] = u.y; key[k + 2] = u.z; key[k + 3] = u.w;
+    }
   } else {
 #pragma unroll
-    for (int k = 0; k < kRleItems; ++k) key[k] = p0 + k < N ? a.keys[p0 + k] : 0u;
+    for (int k = 0; k < ITEMS; ++k) key[k] = p0 + k < N ? a.keys[p0 + k] : 0u;
   }
   const uint32_t prev = (p0 > 0 && p0 <= N) ? a.keys[p0 - 1] : 0u;
   uint32_t heads = 0;  // bit k: position p0+k starts a run
 #pragma unroll
-  for (int k = 0; k < kRleItems; ++k) {
+  for (int k = 0; k < ITEMS; ++k) {
     const uint32_t before = k == 0 ? prev : key[k - 1];
     if (p0 + k < N && (p0 + k == 0 || key[k] != before)) heads |= 1u << k;
     if (p0 + k == N - 1) s_end_key = key[k];
@@ -103,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   {
     uint32_t h = h0;
 #pragma unroll
-    for (int k = 0; k < kRleItems; ++k) {
+    for (int k = 0; k < ITEMS; ++k) {
       if (heads & (1u << k)) {
         s_head_pos[h] = p0 + k;
         if (h == n_heads - 1) s_last_key = key[k];
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   __syncthreads();
   // end of the tile's last run (it may continue into later tiles)
   if (warp == 0 && n_heads > 0) {
-    const uint32_t tile_end = min(i0 + (uint32_t)kRleTile, N);
+    const uint32_t tile_end = min(i0 + TILE, N);
     const uint32_t e = run_end_search(a.keys, N, tile_end, s_last_key);
     if (lane == 0) s_head_pos[n_heads] = e;
   }
@@ -125,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   {
     uint32_t h = h0;
 #pragma unroll
-    for (int k = 0; k < kRleItems; ++k) {
+    for (int k = 0; k < ITEMS; ++k) {
       if (heads & (1u << k)) {
         const uint32_t SL = s_head_pos[h + 1] - s_head_pos[h];
         if (SL >= a.thr) {
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   bool overflow = false;
   uint32_t h = h0;
 #pragma unroll
-  for (int k = 0; k < kRleItems; ++k) {
+  for (int k = 0; k < ITEMS; ++k) {
     if (heads & (1u << k)) {
       const uint32_t start = s_head_pos[h], end = s_head_pos[h + 1];
       if (r < N) {
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
     }
   }
   if (overflow) raise_error(a.ctl, a.sticky, kErrCapacity);
-  if (i0 + kRleTile >= N && threadIdx.x == 0) {  // the last tile knows every total
+  if (i0 + TILE >= N && threadIdx.x == 0) {  // the last tile knows every total
     const uint32_t U = s_base[0] + n_heads;
     if (U <= N) {
       a.ctl->num_runs = U;
@@ -197,27 +206,46 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   }
 }
 
+const void* runs_fn(bool multi, int items) {
+  if (items == 16)
+    return multi ? reinterpret_cast<const void*>(&k_runs<true, 16>) : reinterpret_cast<const void*>(&k_runs<false, 16>);
+  return multi ? reinterpret_cast<const void*>(&k_runs<true, 8>) : reinterpret_cast<const void*>(&k_runs<false, 8>);
+}
+
+size_t runs_smem_bytes(int items, uint32_t S) { return items == 16 ? runs_smem<16>(S) : runs_smem<8>(S); }
+
 }  // namespace
 
-int runs_capacity(int S, int sms) {
+// Sorted keys per thread: 8 (2048-key tiles) up to 2^21 lookups, 16 above
+// (half as many tiles, so half as many look-back steps and run-end searches).
+int runs_items_for(int64_t N) { return N <= (int64_t)(1 << 21) ? 8 : 16; }
+
+cudaError_t runs_configure() {
+  cudaError_t e = cudaSuccess;
+  for (int multi = 0; multi < 2 && e == cudaSuccess; ++multi)
+    for (int items : {8, 16})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(runs_fn(multi != 0, items), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)runs_smem_bytes(items, kMaxT));
+  return e;
+}
+
+int runs_capacity(int S, int items, int sms) {
   int blocks = 0;
-  const void* fn = S > 1 ? reinterpret_cast<const void*>(&k_runs<true>) : reinterpret_cast<const void*>(&k_runs<false>);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, S > 1 ? (S + 1) * sizeof(uint32_t) : 0) !=
-      cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, runs_fn(S > 1, items), kThreads,
+                                                    runs_smem_bytes(items, (uint32_t)S)) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return blocks * sms;
 }
 
-cudaError_t launch_runs(const RunsArgs& a, cudaStream_t s, bool pdl) {
-  const unsigned grid = (unsigned)((a.N + kRleTile - 1) / kRleTile);
+cudaError_t launch_runs(const RunsArgs& a, int items, cudaStream_t s, bool pdl) {
+  const unsigned grid = (unsigned)((a.N + (int64_t)kThreads * items - 1) / ((int64_t)kThreads * items));
   RunsArgs arg = a;
   void* args[] = {&arg};
-  const void* fn = a.S > 1 ? reinterpret_cast<const void*>(&k_runs<true>)
-                           : reinterpret_cast<const void*>(&k_runs<false>);
-  return launch_kernel(fn, dim3(grid), dim3(kThreads), a.S > 1 ? (a.S + 1) * sizeof(uint32_t) : 0, s,
-                       args, pdl);
+  return launch_kernel(runs_fn(a.S > 1, items), dim3(grid), dim3(kThreads), runs_smem_bytes(items, a.S), s, args,
+                       pdl);
 }
 
 }  // namespace embbwd

@@ -71,6 +71,22 @@ def test_pooled_variants(opt, pooling, weighted, wdt):
     run_and_check(w)
 
 
+@pytest.mark.parametrize("opt", [synth.SGD, synth.ROWWISE_ADAGRAD])
+@pytest.mark.parametrize("pooling,weighted", [(synth.SUM, False), (synth.SUM, True), (synth.MEAN, False),
+                                              (synth.MEAN, True)])
+def test_repeats_within_bags(opt, pooling, weighted):
+    # bags that hit a few rows dozens of times: long runs made of chains of one
+    # (row, bag), crossing the 2048-key tiles of the run-length pass
+    rows = [50, 3000]
+    w = custom(21, rows, [16, 64], 64, lambda r, T, B: r.integers(0, 300, (T, B)),
+               ids_fn=lambda r, t, n: np.where(r.random(n) < 0.7, r.integers(0, 3, n),
+                                               r.integers(0, rows[t], n)).astype(np.int64),
+               optimizer=opt, pooling=pooling, weighted=weighted, weight_dtype=synth.F16,
+               momentum_init=0.5 if opt == synth.ROWWISE_ADAGRAD else 0.0)
+    assert w.N > 4 * 2048
+    run_and_check(w)
+
+
 @pytest.mark.parametrize("gdt", [synth.F16, synth.BF16])
 def test_half_precision_grad(gdt):
     w = custom(4, [500, 700], [32, 128], 128, lambda r, T, B: r.integers(1, 30, (T, B)),
