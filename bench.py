@@ -89,6 +89,12 @@ def host_arrays(w):
     return conv(w.indices), conv(w.offsets), conv(w.grad_output), conv(w.per_sample_weights)
 
 
+def radix_passes(w):
+    """Radix passes of the sort: the row index of the largest table in digits of at most 9 bits."""
+    row_bits = max(int(np.ceil(np.log2(max(int(np.max(w.rows)), 2)))), 1)
+    return min(-(-row_bits // 9), 4)
+
+
 def algorithmic_bytes(w, variant="update"):
     """Minimal bytes of one step: int64 indices, the gradient row read per lookup,
     and one read + one write of every unique row (and its fp32 state for Adagrad:
@@ -557,7 +563,7 @@ def run_shard(args):
         "cpu_baseline": cpu,
         # bucketize: count, three scan phases, scatter; merge: bases, copy; backward:
         # histogram, radix passes, run-length, reduce
-        "gpu_launches": K * (5 + 2 + 3 + -(-max(int(hsc[-1] - 1).bit_length(), 1) // 8)),
+        "gpu_launches": K * (5 + 2 + 3 + min(-(-max(int(np.max(np.diff(hsc)) - 1).bit_length(), 1) // 9), 4)),
         "clocks": clocks.summary(),
     }, default=float))
     E.emb_plan_destroy(plan)
@@ -700,8 +706,7 @@ def main():
     names = ["linearise_hist", "radix_sort", "run_length", "-", "reduce_update"]
     if atomic:
         names = ["index_check", "-", "-", "-", "atomic_scatter"]
-    total_bits = int(np.ceil(np.log2(max(int(w.hash_size_cumsum[-1]), 2))))
-    passes = (total_bits + 7) // 8
+    passes = radix_passes(w)
     # launches per stage: the dominant kernel is the one with the longest launch
     launches = [1, 0 if atomic else passes, 0 if atomic else 1, 0, 1]
     per_launch = [t / n if n else 0.0 for t, n in zip(stage, launches)]

@@ -76,12 +76,18 @@ struct emb_plan {
     uint32_t* d_segkeys = nullptr;  // hash_size_cumsum of each segment's first table, then the total
   } split[2];
   int key_bits = 1;
+  int passes = 1, rbits = 1;      // radix passes over row indices and their digit bits
+  int radix = 128;                // buckets of the sort kernels for rbits
+  uint32_t max_pass_tiles = 0;    // upper bound on the tiles of a pass (all call sizes)
   std::vector<uint32_t> hsc;
   std::vector<int32_t> Do;
   DevProps props{};
 
   void* arena = nullptr;
   Ctl* ctl = nullptr;
+  uint32_t* thist = nullptr;     // [T][passes][radix] digit counts per table, cleared with ctl
+  size_t clear_bytes = 0;        // bytes from ctl to the end of thist
+  PassTile* tile_map = nullptr;  // [max_pass_tiles]
   uint32_t* sticky = nullptr;
   uint32_t* d_hsc = nullptr;
   int32_t* d_Do = nullptr;
@@ -196,17 +202,20 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   if (p->seq >= (1u << 28)) p->seq = 0;  // epochs stay distinct from the zero-initialised words
   const DecodeArgs d = decode_args(p, indices, offsets, psw, N, B, mean);
   const int tile = (int)sort_tile_for(N), ptile = (int)pass_tile_for(N);
-  const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
+  const int passes = p->passes;
   const bool wide = vk == VK_BAG_SCALED;
   const LookbackCfg lb0{p->status, epoch, kSpinLimit, (p->flags & EMB_FLAG_DEBUG_FORCE_TIMEOUT) ? 1u : 0u};
   const bool pdl = !(p->flags & EMB_FLAG_NO_PDL);
 
   EMB_TRY(record(p, 0, s));
-  EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));
+  EMB_CUDA(cudaMemsetAsync(p->ctl, 0, p->clear_bytes, s));  // control block and per-table histograms
   // the linearised pairs go to buffer 1, which the first pass reads
-  HistArgs ha{d, p->ctl, p->sticky, passes, tile, p->keys[1], p->vals[1]};
+  HistArgs ha{d,           p->ctl,       p->sticky, passes, tile, p->keys[1], p->vals[1],
+              p->thist,    p->tile_map,  p->rbits,  ptile,  p->max_pass_tiles};
   EMB_CUDA(launch_hist(ha, vk, p->T, s, pdl));
   EMB_TRY(record(p, 1, s));
+  // tiles of a pass: at most one partial tile per table on top of N / ptile
+  const unsigned pgrid = (unsigned)((N + ptile - 1) / ptile + p->T);
   for (int pass = 0; pass < passes; ++pass) {
     PassArgs pa;
     pa.N = N;
@@ -219,10 +228,14 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_in = p->vals[in];
     pa.keys_out = p->keys[out];
     pa.vals_out = p->vals[out];
+    pa.thist = p->thist;
+    pa.tile_map = p->tile_map;
+    pa.hsc = p->d_hsc;
     pa.pass = pass;
-    pa.shift = pass * kRadixBits;
-    pa.ordered = (N + ptile - 1) / ptile <= p->pass_cap[pass_tile_class(ptile)][wide ? 1 : 0];
-    EMB_CUDA(launch_sort_pass(pa, wide, ptile, s, pdl));
+    pa.passes = passes;
+    pa.rbits = p->rbits;
+    pa.ordered = (int)pgrid <= p->pass_cap[pass_tile_class(ptile)][wide ? 1 : 0];
+    EMB_CUDA(launch_sort_pass(pa, wide, ptile, pgrid, s, pdl));
   }
   const int fin = (passes - 1) & 1;
   EMB_TRY(record(p, 2, s));
@@ -389,6 +402,14 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   const uint64_t total_rows = (uint64_t)hash_size_cumsum[T];
   p->key_bits = 1;
   while (p->key_bits < 32 && ((uint64_t)1 << p->key_bits) < total_rows) ++p->key_bits;
+  {  // the passes sort row indices within tables: bits of the largest table's rows
+    int64_t max_rows = 1;
+    for (int32_t t = 0; t < T; ++t) max_rows = std::max<int64_t>(max_rows, hash_size_cumsum[t + 1] - hash_size_cumsum[t]);
+    int row_bits = 1;
+    while (row_bits < 32 && ((int64_t)1 << row_bits) < max_rows) ++row_bits;
+    radix_plan(row_bits, &p->passes, &p->rbits);
+    p->radix = radix_buckets(p->rbits);
+  }
   p->hsc.resize(T + 1);
   p->Do.assign(D_offsets, D_offsets + T + 1);
   for (int32_t t = 0; t <= T; ++t) p->hsc[t] = (uint32_t)hash_size_cumsum[t];
@@ -434,8 +455,17 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
 
   // ---- scratch sizes
   const uint64_t N = (uint64_t)std::max<int64_t>(max_N, 1);
-  const uint64_t sort_tiles = std::max<uint64_t>((N + 1023) / 1024, 1);  // smallest tile is 1024
-  const uint64_t status_words = std::max<uint64_t>(sort_tiles * kRadix, (N + kRleTile - 1) / kRleTile * 4);
+  {  // the most tiles any call up to max_N gives a pass (each tile class up to its largest N)
+    uint64_t tiles = 0;
+    for (int64_t n : {std::min<int64_t>((int64_t)N, (int64_t)1 << 17), std::min<int64_t>((int64_t)N, (int64_t)1 << 21),
+                      (int64_t)N}) {
+      const uint64_t pt = pass_tile_for(n);
+      tiles = std::max<uint64_t>(tiles, ((uint64_t)n + pt - 1) / pt);
+    }
+    p->max_pass_tiles = (uint32_t)(tiles + (uint64_t)T + 1);
+  }
+  const uint64_t status_words =
+      std::max<uint64_t>((uint64_t)p->max_pass_tiles << p->rbits, (N + kRleTile - 1) / kRleTile * 4);
   p->cap_long = (uint32_t)(N / p->thr + 1);
   // Slices (row chunk x slice) the reduce cuts the long runs into: at most
   // warps + C with one slice per warp; with more, at most 44 * warps + C and at
@@ -455,7 +485,9 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   void* tmp_sticky = nullptr;
   Seg segs[] = {
       {&tmp_ctl, sizeof(Ctl)},
+      {reinterpret_cast<void**>(&p->thist), (size_t)T * p->passes * p->radix * sizeof(uint32_t)},
       {&tmp_sticky, sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->tile_map), (size_t)p->max_pass_tiles * sizeof(PassTile)},
       {reinterpret_cast<void**>(&p->d_hsc), (T + 1) * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->d_Do), (T + 1) * sizeof(int32_t)},
       {reinterpret_cast<void**>(&p->d_wo), T * sizeof(int64_t)},
@@ -493,6 +525,8 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   }
   p->ctl = static_cast<Ctl*>(tmp_ctl);
   p->sticky = static_cast<uint32_t*>(tmp_sticky);
+  p->clear_bytes = (size_t)(reinterpret_cast<char*>(p->thist) - reinterpret_cast<char*>(p->ctl)) +
+                   (size_t)T * p->passes * p->radix * sizeof(uint32_t);
 
   std::vector<int64_t> mo(T);
   for (int32_t t = 0; t < T; ++t) mo[t] = momentum_offsets ? momentum_offsets[t] : hash_size_cumsum[t];
@@ -515,7 +549,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     const int tiles[3] = {kThreads * 4, kThreads * 8, kThreads * 16};
     for (int c = 0; c < 3; ++c)
       for (int wide = 0; wide < 2; ++wide)
-        p->pass_cap[c][wide] = sort_pass_capacity(wide != 0, tiles[c], p->props.sms);
+        p->pass_cap[c][wide] = sort_pass_capacity(wide != 0, tiles[c], p->rbits, p->props.sms);
     for (int opt = 0; opt < 2; ++opt)
       for (int it = 0; it < 2; ++it)
         p->runs_cap[opt][it] = runs_capacity((int)p->split[opt].segs.size() - 1, it ? 16 : 8, p->props.sms);

@@ -3,11 +3,14 @@
 // Pipeline of one sorted call (all stream-ordered, no host synchronisation):
 //   memset(ctl) -> k_hist -> k_sort_pass x passes -> k_runs -> k_reduce
 //   k_hist      linearises every lookup (hash_size_cumsum[t] + idx), checks it
-//               against its table, validates the CSR offsets and builds the digit
-//               histograms of all radix passes in one read of the indices.
-//   k_sort_pass one LSD radix pass (8-bit digits) with decoupled look-back; the
-//               first pass recomputes the keys from the indices instead of
-//               reading a materialised key array.
+//               against its table, validates the CSR offsets and builds, per
+//               table, the digit histograms of all radix passes over the row
+//               index in one read of the indices; its block 0 lays out the
+//               passes' tiles on the tables' segments.
+//   k_sort_pass one LSD radix pass over the row index (5..9-bit digits) with
+//               decoupled look-back, each table's segment sorted on its own
+//               (lookups arrive table-major, so the segments are already in key
+//               order and only the row bits need sorting).
 //   k_runs      run-length encode of the sorted keys (unique keys, run starts,
 //               number of runs) fused with the ordered compaction of runs with
 //               >= max_segment_length_per_warp lookups (with the prefix sum of
@@ -30,9 +33,8 @@ namespace embbwd {
 
 constexpr int kThreads = 256;  // every kernel uses 8 warps per block
 constexpr int kWarps = kThreads / 32;
-constexpr int kRadixBits = 8;
-constexpr int kRadix = 1 << kRadixBits;
-constexpr int kMaxPasses = 4;  // 32-bit keys
+constexpr int kMaxRadixBits = 9;  // digits of 1..9 bits: 2..512 buckets per pass
+constexpr int kMaxPasses = 4;     // 32-bit row indices
 constexpr int kRleItems = 8;   // sorted keys per thread of k_runs (16 for large batches)
 constexpr int kRleTile = kThreads * kRleItems;  // smallest k_runs tile
 constexpr int kMaxT = 4096;
@@ -53,8 +55,8 @@ struct Ctl {
   uint32_t num_runs;
   uint32_t num_long;
   uint32_t long_lookups;  // lookups in long runs
-  uint32_t pad[4];
-  uint32_t hist[kMaxPasses][kRadix];
+  uint32_t pass_tiles;    // tiles of every radix pass (the tiles of all tables' segments)
+  uint32_t pad[3];
   // Reduce: long-run slices handed out dynamically, one counter per warp index
   // of a block (each in its own 128-byte line).
   uint32_t slice_ctr[kWarps][32];
@@ -91,6 +93,12 @@ struct DecodeArgs {
   int mean;
 };
 
+// A tile of a radix pass: sorted positions [i0, i1) of table t, whose segment's
+// first tile is `first`.
+struct PassTile {
+  uint32_t t, i0, i1, first;
+};
+
 struct HistArgs {
   DecodeArgs d;
   Ctl* ctl;
@@ -99,6 +107,11 @@ struct HistArgs {
   int tile;              // lookups per block
   uint32_t* keys_out;    // linear keys in lookup order (not written when only checking)
   void* vals_out;        // payloads in lookup order
+  uint32_t* thist;       // [T][passes][radix] digit counts of the row index, per table (zeroed)
+  PassTile* tile_map;    // written by block 0: the passes' tiles, table by table
+  int rbits;             // digit bits of a pass (radix = 1 << rbits, <= the kernel's bucket count)
+  int ptile;             // lookups per tile of the passes
+  uint32_t tile_cap;     // entries of tile_map (malformed offsets can ask for more; they are cut)
 };
 
 struct PassArgs {
@@ -110,8 +123,12 @@ struct PassArgs {
   const void* vals_in;
   uint32_t* keys_out;
   void* vals_out;
+  const uint32_t* thist;      // [T][passes][radix]
+  const PassTile* tile_map;   // [ctl->pass_tiles]
+  const uint32_t* hsc;        // [T+1]
   int pass;
-  int shift;
+  int passes;
+  int rbits;                  // the digit of pass p is bits [p*rbits, (p+1)*rbits) of the row index
   int ordered;  // 1: tile = blockIdx.x (the whole grid fits on the GPU at once)
 };
 
@@ -296,52 +313,78 @@ __device__ __forceinline__ void block_excl_scan2(uint32_t v0, uint32_t v1, uint3
   *t1 = s1;
 }
 
-// Decoupled look-back for one channel: publishes this tile's aggregate, walks
-// back over predecessors until an inclusive prefix is found, publishes its own
-// inclusive prefix and returns the exclusive one. Every wait is bounded: after
-// spin_limit polls the tile raises kErrTimeout and carries on with what it has
-// (its successors never wait forever, and nothing is updated in that call).
-__device__ __forceinline__ uint32_t lookback_channel(const LookbackCfg& lb, uint32_t tile,
-                                                     uint32_t channels, uint32_t c, uint32_t agg,
-                                                     Ctl* ctl, uint32_t* sticky) {
-  uint64_t* st = lb.status + (size_t)tile * channels + c;
+// Decoupled look-back over DPT channels at once (the DPT digits a thread owns):
+// publishes this tile's aggregates, walks back over the predecessors down to
+// tile `first` (the first tile of the segment: nothing before it counts) until
+// an inclusive prefix is found, publishes its own inclusive prefixes and returns
+// the exclusive ones in excl. Channels c >= channels are skipped. Every wait is
+// bounded: after spin_limit polls the tile raises kErrTimeout and carries on with
+// what it has (its successors never wait forever, and nothing is updated in that
+// call).
+template <int DPT>
+__device__ __forceinline__ void lookback_channels(const LookbackCfg& lb, uint32_t tile, uint32_t first,
+                                                  uint32_t channels, const uint32_t (&c)[DPT],
+                                                  const uint32_t (&agg)[DPT], uint32_t (&excl)[DPT], Ctl* ctl,
+                                                  uint32_t* sticky) {
   const uint64_t tag = (uint64_t)lb.epoch << 32;
-  if (tile == 0) {
-    st_relaxed_u64(st, tag | kFlagInc | agg);
-    return 0;
+  bool live[DPT];
+#pragma unroll
+  for (int q = 0; q < DPT; ++q) {
+    live[q] = c[q] < channels;
+    excl[q] = 0;
+    if (live[q])
+      st_relaxed_u64(lb.status + (size_t)tile * channels + c[q],
+                     tag | (tile == first ? kFlagInc : kFlagAgg) | agg[q]);
   }
-  st_relaxed_u64(st, tag | kFlagAgg | agg);
-  // Windowed walk: kLookbackWindow predecessors are read per poll (independent
-  // loads in flight), so a chain of tiles that published only aggregates is
-  // crossed kLookbackWindow tiles per memory round trip.
+  if (tile == first) return;
+  // Windowed walk: kWin predecessors are read per poll (independent loads in
+  // flight), so a chain of tiles that published only aggregates is crossed kWin
+  // tiles per memory round trip.
   constexpr int kWin = 16;
-  uint32_t excl = 0;
   bool failed = lb.force_timeout != 0;
-  int64_t j = (int64_t)tile - 1;
+  int64_t j[DPT];
+  bool done[DPT];
+#pragma unroll
+  for (int q = 0; q < DPT; ++q) {
+    j[q] = (int64_t)tile - 1;
+    done[q] = !live[q];
+  }
   uint32_t polls = 0;
-  while (!failed && j >= 0) {
-    uint64_t w[kWin];
+  while (!failed) {
+    bool all = true, progress = true;
 #pragma unroll
-    for (int k = 0; k < kWin; ++k)
-      w[k] = j - k >= 0 ? ld_relaxed_u64(lb.status + (size_t)(j - k) * channels + c) : (tag | kFlagInc);
-    int k = 0;
-    bool done = false;
+    for (int q = 0; q < DPT; ++q) {
+      if (done[q]) continue;
+      uint64_t w[kWin];
 #pragma unroll
-    for (int q = 0; q < kWin; ++q) {
-      if (k != q) continue;  // an earlier word was not ready
-      const uint64_t x = w[q];
-      if ((uint32_t)(x >> 32) != lb.epoch || !(x & (kFlagAgg | kFlagInc))) continue;
-      excl += (uint32_t)x & kCountMask;
-      if (x & kFlagInc) {
-        done = true;
-        k = kWin + 1;
-      } else {
-        k = q + 1;
+      for (int k = 0; k < kWin; ++k)
+        w[k] = j[q] - k >= (int64_t)first ? ld_relaxed_u64(lb.status + (size_t)(j[q] - k) * channels + c[q])
+                                          : (tag | kFlagInc);
+      int m = 0;
+      bool inc = false;
+#pragma unroll
+      for (int k = 0; k < kWin; ++k) {
+        if (m != k) continue;  // an earlier word was not ready
+        const uint64_t x = w[k];
+        if ((uint32_t)(x >> 32) != lb.epoch || !(x & (kFlagAgg | kFlagInc))) continue;
+        excl[q] += (uint32_t)x & kCountMask;
+        if (x & kFlagInc) {
+          inc = true;
+          m = kWin + 1;
+        } else {
+          m = k + 1;
+        }
       }
+      if (inc) {
+        done[q] = true;
+        continue;
+      }
+      j[q] -= m;  // first tile not yet published (or the next window)
+      all = false;
+      if (m < kWin) progress = false;
     }
-    if (done) break;
-    j -= k;  // first tile not yet published (or the next window)
-    if (k < kWin) {
+    if (all) break;
+    if (!progress) {
       if (++polls > lb.spin_limit) {
         failed = true;
         break;
@@ -350,8 +393,10 @@ __device__ __forceinline__ uint32_t lookback_channel(const LookbackCfg& lb, uint
     }
   }
   if (failed) raise_error(ctl, sticky, kErrTimeout);
-  st_relaxed_u64(st, tag | kFlagInc | ((excl + agg) & kCountMask));
-  return excl;
+#pragma unroll
+  for (int q = 0; q < DPT; ++q)
+    if (live[q])
+      st_relaxed_u64(lb.status + (size_t)tile * channels + c[q], tag | kFlagInc | ((excl[q] + agg[q]) & kCountMask));
 }
 
 // Warp-wide decoupled look-back for one channel: all 32 lanes of a warp call
@@ -567,11 +612,16 @@ inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, size_t s
 size_t sort_tile_for(int64_t N);  // lookups per block of the histogram kernel
 size_t pass_tile_for(int64_t N);  // lookups per block of the radix passes: 1024, 2048 or 4096
 int pass_tile_class(int tile);    // 0, 1, 2 for those
+// Radix passes over row indices of `row_bits` bits: passes and digit bits.
+void radix_plan(int row_bits, int* passes, int* rbits);
+// Buckets of the kernels that serve digits of rbits bits (128, 256 or 512).
+int radix_buckets(int rbits);
 // first_kind: the ValueKind of the pairs to write, or -1 to only check indices and offsets.
 cudaError_t launch_hist(const HistArgs& a, int first_kind, int T, cudaStream_t s, bool pdl);
-cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, cudaStream_t s, bool pdl);
+// grid: tiles of the pass (an upper bound: blocks past ctl->pass_tiles exit).
+cudaError_t launch_sort_pass(const PassArgs& a, bool wide_vals, int tile, unsigned grid, cudaStream_t s, bool pdl);
 // Blocks of the pass kernel (and of k_runs) that fit on the GPU at once.
-int sort_pass_capacity(bool wide_vals, int tile, int sms);
+int sort_pass_capacity(bool wide_vals, int tile, int rbits, int sms);
 int runs_capacity(int S, int items, int sms);
 cudaError_t sort_configure(const DevProps& p);
 
