@@ -570,6 +570,117 @@ def run_shard(args):
     E.emb_shard_destroy(sh)
 
 
+def run_shard_dist(args, device=None, ops_factory=None, workload=None):
+    """The row-sharded step over WORLD_SIZE ranks (one per GPU, NCCL): every rank
+    has its own batch and owns the rows congruent to its rank modulo W of every
+    table; per step the lookups are routed to their owners (bucketize, three
+    all-to-alls, merge), the forward runs on the owners and a reduce-scatter
+    returns each rank its bags, and the backward all-gathers grad_output and
+    updates each owner's rows. Each stage is timed on its own (the max over
+    ranks); value = all ranks' lookups / the max step time.
+
+    device / ops_factory / workload let the CPU test drive the same code over gloo
+    with other implementations of the library steps (None: the GPU and the library)."""
+    import torch
+    import torch.distributed as dist
+    from sparse_embedding_bag_gb300 import embbwd as E
+    from sparse_embedding_bag_gb300 import shard as S
+    from sparse_embedding_bag_gb300 import synth
+    world = int(os.environ["WORLD_SIZE"])
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    on_gpu = device is None
+    if on_gpu:
+        torch.cuda.set_device(local)
+        device = f"cuda:{local}"
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        from sparse_embedding_bag_gb300 import build as b
+        b.build()
+        E.load()
+    elif not dist.is_initialized():
+        dist.init_process_group("gloo")
+    name = workload or args.workload
+    if name not in ("dlrm", "tiny"):
+        raise SystemExit("--op shard needs a workload whose table shapes do not depend on the seed (dlrm, tiny)")
+    w = synth.BY_NAME[name](rank)  # this rank's batch; every rank has the same table shapes
+    T, B = w.T, w.B
+    n_all = torch.tensor([w.N], dtype=torch.int64, device=device)
+    dist.all_reduce(n_all)
+    max_N = int(n_all.item())  # an owner receives at most every rank's lookups
+    sb = S.RowShardedBags(w.rows, w.dims, rank, world, B, max_N, cyclic=True, device=device,
+                          weight_dtype=w.weight_dtype, grad_dtype=w.grad_dtype,
+                          ops=None if ops_factory is None else ops_factory(w, rank, world))
+    own = S.owned_rows(w.rows, None, rank, world, cyclic=True)
+    wl = torch.from_numpy(np.concatenate([w.weights[(w.weights_offsets[t] + own[t][:, None] * w.dims[t] +
+                                                     np.arange(w.dims[t])).reshape(-1)]
+                                          for t in range(T)])).to(device)
+    ml = torch.zeros(int(sb.hsc[-1]), dtype=torch.float32, device=device)
+    idx = torch.from_numpy(w.indices).to(device)
+    off = torch.from_numpy(w.offsets).to(device)
+    grad = torch.from_numpy(np.ascontiguousarray(w.grad_output)).to(device)
+    sync = torch.cuda.synchronize if on_gpu else (lambda: None)
+
+    def step(times=None):
+        t0 = time.perf_counter()
+        routed = sb.route(idx, off, w.N, B)
+        sync()
+        t1 = time.perf_counter()
+        sb.forward(wl, routed)
+        sync()
+        t2 = time.perf_counter()
+        if w.optimizer == synth.SGD:
+            sb.backward_sgd(wl, routed, grad, w.lr)
+        else:
+            sb.backward_rowwise_adagrad(wl, ml, routed, grad, w.lr, w.eps)
+        sync()
+        t3 = time.perf_counter()
+        if times is not None:
+            times.append((t1 - t0, t2 - t1, t3 - t2))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    dist.barrier()
+    sync()
+    times = []
+    with ClockSampler(local) if on_gpu else _NoClocks() as clocks:
+        t_start = time.perf_counter()
+        for _ in range(args.steps):
+            step(times)
+        sync()
+        dist.barrier()
+        wall = time.perf_counter() - t_start
+    mean = np.mean(np.array(times), axis=0) * 1e3  # ms: exchange, forward, backward
+    stats = torch.tensor([wall * 1e3 / args.steps, *mean.tolist()], dtype=torch.float64, device=device)
+    dist.all_reduce(stats, op=dist.ReduceOp.MAX)
+    ms, ex_ms, fw_ms, bw_ms = (float(x) for x in stats.tolist())
+    sb.close()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "row-sharded embedding step (route, forward, backward with update): "
+                      "all ranks' lookups/sec",
+            "op": "shard", "value": int(n_all.item()) / (ms * 1e-3), "unit": "lookups/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": DESCR[name] + " per rank", "parallelism": f"row-sharded, {world} ranks",
+                       "row_map": "rows modulo W", "N_all_ranks": int(n_all.item()),
+                       "collectives": "all_to_all_single x3, reduce_scatter_tensor, all_gather_into_tensor"},
+            "stage_ms": {"exchange": ex_ms, "forward": fw_ms, "backward": bw_ms},
+            "e2e": None, "gpu_launches": args.steps * (7 + 1 + 3 + radix_passes(w)) if on_gpu else 0,
+            "clocks": clocks.summary(),
+        }, default=float))
+
+
+class _NoClocks:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+    def summary(self):
+        return None
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -577,6 +688,8 @@ def main():
     if args.op == "fwd":
         return run_forward(args)
     if args.op == "shard":
+        if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            return run_shard_dist(args)
         return run_shard(args)
     import torch
     import torch.distributed as dist

@@ -374,11 +374,14 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     // 16-byte vectors each lane holds of a row (rows wider than kv*32 vectors are
     // cut into chunks). Narrow rows take more than they need, so that a row spans
     // only a few lanes and a warp works on several short runs at once (the short
-    // runs of skewed batches are mostly single lookups). Measured on GB300: kv = 8
-    // costs too much occupancy, so rows of 33-64 vectors stay at kv = 2, and SGD
-    // cuts rows wider than 64 vectors into chunks of 64 (kv = 2). Row-wise Adagrad
-    // needs the whole row in one warp for its norm, so it widens kv instead.
-    if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 16 ? 2 : nvec <= 32 ? 4 : 2;
+    // runs of skewed batches are mostly single lookups), and each lane has more
+    // loads in flight. Measured on GB300: rows of 9-32 vectors run fastest at
+    // kv = 4 (the large skewed workload's reduce: 8.6 ms at kv = 1, 7.4 at 2, 6.1
+    // at 4; the DLRM-like one 30.9 us at 2, 29.2 at 4); kv = 8 costs too much
+    // occupancy, so rows of 33-64 vectors stay at kv = 2, and SGD cuts rows wider
+    // than 64 vectors into chunks of 64 (kv = 2). Row-wise Adagrad needs the
+    // whole row in one warp for its norm, so it widens kv instead.
+    if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 32 ? 4 : 2;
     else sp.kv = opt == 0 ? 2 : nvec <= 128 ? 4 : 8;
     sp.C = (uint32_t)((nvec + sp.kv * 32 - 1) / (sp.kv * 32));
     auto shape = [&](int32_t t) {  // (chunks per row, lanes per lookup) of table t
