@@ -43,9 +43,16 @@ DESCR = {
              "Zipf(1.2) ids, sum, row-wise Adagrad",
 }
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# dominant kernel, from ncu captures of the current kernels; a workload without
-# an entry reports null.
-TRAFFIC = {("dlrm", "reduce_update"): 21_136_640}
+# dominant kernel, from ncu captures of the current kernels (the large workload at
+# full size, in the metric's single pass; the others from full section captures);
+# a workload without an entry reports null.
+TRAFFIC = {
+    ("large", "reduce_update"): 12_570_000_000 + 2_480_000_000,
+    ("dlrm", "reduce_update"): 21_118_208 + 1_536,
+    ("mixed", "reduce_update"): 699_678_720 + 165_902_848,
+    ("lm", "reduce_update"): 399_276_288 + 86_008_832,
+    ("lm", "atomic_scatter"): 418_241_536 + 115_250_432,
+}
 
 
 def parse():
