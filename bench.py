@@ -47,7 +47,6 @@ DESCR = {
 # full size, in the metric's single pass; the others from full section captures);
 # a workload without an entry reports null.
 TRAFFIC = {
-    ("large", "reduce_update"): 12_570_000_000 + 2_480_000_000,
     ("dlrm", "reduce_update"): 21_118_208 + 1_536,
     ("mixed", "reduce_update"): 699_678_720 + 165_902_848,
     ("lm", "reduce_update"): 399_276_288 + 86_008_832,

@@ -471,13 +471,14 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       std::max<uint64_t>((uint64_t)p->max_pass_tiles << p->rbits, (N + kRleTile - 1) / kRleTile * 4);
   p->cap_long = (uint32_t)(N / p->thr + 1);
   // Slices (row chunk x slice) the reduce cuts the long runs into: at most
-  // warps + C with one slice per warp; with more, at most 44 * warps + C and at
-  // most C * (N / kMinSlice + 2). Each has a head and a tail partial row of kv*32
-  // vectors.
+  // warps + C with one slice per warp; with more (slices of at least
+  // pow2ceil(lookups per warp / 32), the last quarter of the lookups in slices 4x
+  // smaller), at most 56 * warps + 5 * C, and at most C * (N / kMinSlice + 2).
+  // Each has a head and a tail partial row of kv*32 vectors.
   {
     const uint64_t warps = (uint64_t)max_grid * kWarps;
     const uint64_t C = std::max(p->split[0].C, p->split[1].C);
-    p->cap_slices = (uint32_t)(warps + C + std::min<uint64_t>(48 * warps, C * (N / kMinSlice + 2)));
+    p->cap_slices = (uint32_t)(warps + 5 * C + std::min<uint64_t>(64 * warps, C * (N / kMinSlice + 2)));
   }
   const size_t part_row = (size_t)std::max(p->split[0].kv, p->split[1].kv) * 32 * sizeof(float4);
   struct Seg {

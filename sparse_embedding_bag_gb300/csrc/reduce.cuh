@@ -469,9 +469,14 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
   // slice is updated at once; a run cut by slice ends leaves one fp32 partial per
   // piece, combined by the pieces that finish last (atomic counts, no waiting;
   // see piece_arrive) in slice order before the row is updated. Little long-run
-  // work: one slice per warp, assigned statically. Much: about 16 slices per warp,
+  // work: one slice per warp, assigned statically. Much: about 32 slices per warp,
   // handed out through one counter per warp index of a block (slice g belongs to
   // counter g % kWarps), the next one requested while the current one is reduced.
+  // Slices are handed out in key order, so their size sets how many tables'
+  // gradient slabs are live at once: measured on the large skewed workload,
+  // about 16 slices per warp (six tables' slabs, more than L2 holds) gave
+  // 6.16 ms and 15.1 GB of DRAM traffic, about 32 gave 5.89 ms, about 64 gave
+  // 5.93 ms and 10.0 GB.
   const uint32_t NL = *(volatile uint32_t*)&a.ctl->num_long;
   const uint32_t Ltot = *(volatile uint32_t*)&a.ctl->long_lookups;
   if (Ltot > 0) {
@@ -483,10 +488,10 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
       sl.nA = (Ltot + sl.SLA - 1) / sl.SLA;
       sl.LA = Ltot;
     } else {
-      // about 16 slices per warp; with large slices, the last quarter of the
+      // about 32 slices per warp; with large slices, the last quarter of the
       // lookups in slices 4x smaller, so that the warps that take the last
       // slices finish together
-      sl.SLA = max(kMinDynSlice, 1u << (32 - __clz((uint32_t)((per_warp + 15) / 16) - 1)));  // pow2ceil(per_warp / 16)
+      sl.SLA = max(kMinDynSlice, 1u << (32 - __clz((uint32_t)((per_warp + 31) / 32) - 1)));  // pow2ceil(per_warp / 32)
       sl.SLB = sl.SLA >= 256 ? sl.SLA / 4 : sl.SLA;
       sl.nA = (uint32_t)((uint64_t)Ltot * 3 / 4 / sl.SLA);
       sl.LA = sl.nA * sl.SLA;
