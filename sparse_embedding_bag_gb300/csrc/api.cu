@@ -29,7 +29,12 @@ struct NvtxRange {
 };
 
 constexpr uint32_t kSpinLimit = 1u << 22;  // polls before a look-back wait gives up (~1 s)
-constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups per reduce warp slice
+constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups a reduce warp slice can have
+// Fewest long-run lookups per warp slice when there is little long-run work (one
+// slice per warp at most): below it, fewer warps take the long runs and the rest
+// start on the short runs at once. Measured on GB300 (DLRM-like batch, 45 long-run
+// lookups per warp): see the reduce's phase comments.
+constexpr uint32_t kStaticMinSlice = 128;
 constexpr int kStages = 5;
 
 struct DeviceGuard {
@@ -285,7 +290,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.lr = lr;
   r.eps = eps;
   r.thr = p->thr;
-  r.min_slice = kMinSlice;
+  r.min_slice = kStaticMinSlice;
   r.C = p->split[si].C;
   r.grad_out = grad_out;
   r.dense = dense;

@@ -60,6 +60,8 @@ struct Ctl {
   // Reduce: long-run slices handed out dynamically, one counter per warp index
   // of a block (each in its own 128-byte line).
   uint32_t slice_ctr[kWarps][32];
+  // Reduce: short-run rounds claimed dynamically, the same way.
+  uint32_t round_ctr[kWarps][32];
 };
 
 // Sort-value kinds: what travels with each key through the radix passes.

@@ -469,7 +469,9 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
   // slice is updated at once; a run cut by slice ends leaves one fp32 partial per
   // piece, combined by the pieces that finish last (atomic counts, no waiting;
   // see piece_arrive) in slice order before the row is updated. Little long-run
-  // work: one slice per warp, assigned statically. Much: about 32 slices per warp,
+  // work: one slice per warp, of at least min_slice lookups, assigned statically
+  // (with less work than that per warp, fewer warps take the long runs and the
+  // others start on the short runs at once). Much: about 32 slices per warp,
   // handed out through one counter per warp index of a block (slice g belongs to
   // counter g % kWarps), the next one requested while the current one is reduced.
   // Slices are handed out in key order, so their size sets how many tables'
@@ -587,21 +589,34 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
     const uint32_t Lt = 1u << lgt, NT = 32u >> lgt;
     const uint32_t team = lane >> lgt, tl = lane & (Lt - 1);
     const uint32_t tasks = U * C;  // < 2^31 (checked when the plan is made)
-    // the bounds and key of the next round's run are loaded before this round's rows
-    auto meta = [&](uint32_t task, uint32_t& start, uint32_t& end, uint32_t& key) {
-      if (task < tasks) {
+    const uint32_t rounds = (tasks + NT - 1) / NT;
+    // Rounds are claimed in key order, one at a time: round k * kWarps + c from
+    // counter c (the warp's index in its block), so that warps that spent longer
+    // on the long runs take fewer of them; the next round is claimed, and its
+    // run's bounds and key loaded, before this round's rows.
+    uint32_t* ctr = &a.ctl->round_ctr[warp][0];
+    auto claim = [&]() {
+      uint32_t k = 0;
+      if (lane == 0) k = atomicAdd(ctr, 1u);
+      return __shfl_sync(0xffffffffu, k, 0) * (uint32_t)kWarps + warp;
+    };
+    auto meta = [&](uint32_t q, uint32_t& start, uint32_t& end, uint32_t& key) {
+      const uint32_t task = q * NT + team;
+      if (q < rounds && task < tasks) {
         const uint32_t r = C == 1 ? task : task / C;
         start = a.run_start[r];
         end = a.run_start[r + 1];
         key = a.run_key[r];
       }
     };
+    uint32_t q = claim();
     uint32_t n_start = 0, n_end = 0, n_key = 0;
-    meta(gw * NT + team, n_start, n_end, n_key);
-    for (uint32_t base = gw * NT; base < tasks; base += W * NT) {
-      const uint32_t task = base + team;
+    meta(q, n_start, n_end, n_key);
+    while (q < rounds) {
+      const uint32_t task = q * NT + team;
       const uint32_t start = n_start, end = n_end, key = n_key;
-      meta(base + W * NT + team, n_start, n_end, n_key);
+      q = claim();
+      meta(q, n_start, n_end, n_key);
       const uint32_t r = C == 1 ? task : task / C;
       round(task < tasks, start, end, key, kAnyTable, task - r * C, Lt, tl);
     }
