@@ -47,9 +47,10 @@ DESCR = {
 # full size, in the metric's single pass; the others from full section captures);
 # a workload without an entry reports null.
 TRAFFIC = {
-    ("dlrm", "reduce_update"): 21_118_208 + 1_536,
-    ("mixed", "reduce_update"): 699_678_720 + 165_902_848,
-    ("lm", "reduce_update"): 399_276_288 + 86_008_832,
+    ("large", "reduce_update"): 8_444_050_688 + 2_477_037_568,
+    ("dlrm", "reduce_update"): 21_105_152 + 1_792,
+    ("mixed", "reduce_update"): 679_966_464 + 186_059_520,
+    ("lm", "reduce_update"): 399_136_000 + 84_040_448,
     ("lm", "atomic_scatter"): 418_241_536 + 115_250_432,
 }
 

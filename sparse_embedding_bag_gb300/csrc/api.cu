@@ -33,8 +33,8 @@ constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups a reduce w
 // Fewest long-run lookups per warp slice when there is little long-run work (one
 // slice per warp at most): below it, fewer warps take the long runs and the rest
 // start on the short runs at once. Measured on GB300 (DLRM-like batch, 45 long-run
-// lookups per warp): see the reduce's phase comments.
-constexpr uint32_t kStaticMinSlice = 128;
+// lookups per warp): reduce 26.7 us with a floor of 64, 27.3 at 128, 36.0 at 256.
+constexpr uint32_t kStaticMinSlice = 64;
 constexpr int kStages = 5;
 
 struct DeviceGuard {
@@ -384,10 +384,11 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     // kv = 4 (the large skewed workload's reduce: 8.6 ms at kv = 1, 7.4 at 2, 6.1
     // at 4; the DLRM-like one 30.9 us at 2, 29.2 at 4); kv = 8 costs too much
     // occupancy, so rows of 33-64 vectors stay at kv = 2, and SGD cuts rows wider
-    // than 64 vectors into chunks of 64 (kv = 2). Row-wise Adagrad needs the
-    // whole row in one warp for its norm, so it widens kv instead.
+    // than 64 vectors into chunks of 128 (kv = 4; the LM workload's 1024-vector
+    // rows: reduce 114.7 us in chunks of 64, 110.6 in chunks of 128). Row-wise
+    // Adagrad needs the whole row in one warp for its norm, so it widens kv instead.
     if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 32 ? 4 : 2;
-    else sp.kv = opt == 0 ? 2 : nvec <= 128 ? 4 : 8;
+    else sp.kv = opt == 0 ? 4 : nvec <= 128 ? 4 : 8;
     sp.C = (uint32_t)((nvec + sp.kv * 32 - 1) / (sp.kv * 32));
     auto shape = [&](int32_t t) {  // (chunks per row, lanes per lookup) of table t
       const int nv = (D_offsets[t + 1] - D_offsets[t]) / 4;
