@@ -5,6 +5,7 @@
 // (T > 0, B > 0, the embedding-dimension limit, the empty-indices
 // short-circuit) and adds the alignment and capacity checks the vectorised
 // kernels need.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -70,7 +71,8 @@ struct emb_plan {
   uint64_t sr_seed = 0, sr_call = 0;  // stochastic rounding: Philox key, next call number
   int max_D = 0;
   bool uniform_D = true;
-  // How the reduce splits rows, per optimizer (0 SGD, 1 row-wise Adagrad).
+  // How the reduce splits rows: 0 pooled SGD (and the other per-element updates),
+  // 1 row-wise Adagrad, 2 unpooled lookups (see split_index).
   struct RowSplit {
     int kv = 1;                     // 16-byte vectors per lane
     uint32_t C = 1;                 // chunks of kv*32 vectors per row
@@ -79,7 +81,7 @@ struct emb_plan {
     std::vector<uint32_t> segs;
     uint32_t* d_segs = nullptr;
     uint32_t* d_segkeys = nullptr;  // hash_size_cumsum of each segment's first table, then the total
-  } split[2];
+  } split[3];
   int key_bits = 1;
   int passes = 1, rbits = 1;      // radix passes over row indices and their digit bits
   int radix = 128;                // buckets of the sort kernels for rbits
@@ -116,7 +118,7 @@ struct emb_plan {
   // Blocks that fit on the GPU at once: sort pass [tile class][wide payload], k_runs
   // [split][8 or 16 keys per thread].
   int pass_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};  // [pass tile class][wide values]
-  int runs_cap[2][2] = {{0, 0}, {0, 0}};
+  int runs_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};
   int fwd_grid[3] = {0, 0, 0};  // forward kernel grid per output type (0: not set up yet)
   cudaStream_t last_stream = nullptr;
   int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
@@ -130,8 +132,13 @@ struct emb_plan {
 
 namespace {
 
+// Row split of a call: row-wise Adagrad keeps whole rows in one warp; unpooled
+// lookups (whole-warp rows of one table width, no bag to share) and pooled
+// per-element updates split rows differently (see the plan).
+int split_index(int opt, int vk) { return opt == 1 ? 1 : (vk == VK_NOBAG ? 2 : 0); }
+
 const void* reduce_fn(const emb_plan* p, int opt, int vk) {
-  const emb_plan::RowSplit& sp = p->split[opt == 1 ? 1 : 0];  // elementwise updates split rows like SGD
+  const emb_plan::RowSplit& sp = p->split[split_index(opt, vk)];
   const ReduceKey k{static_cast<int>(p->gdt), opt, vk, sp.kv, sp.segs.size() > 2};
   static const void* (*const entry[3][3])(const ReduceKey&) = {
       {reduce_kernel_f32_f32, reduce_kernel_f32_f16, reduce_kernel_f32_bf16},
@@ -202,7 +209,7 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
                       const int64_t* indices, const int64_t* offsets, int64_t N, int32_t B,
                       const float* psw, const void* grad, int mean, float lr, float eps,
                       void* grad_out, int dense, cudaStream_t s) {
-  const int si = opt == 1 ? 1 : 0;  // row split of this optimizer
+  const int si = split_index(opt, vk);
   const uint32_t epoch = ++p->seq * 8u;
   if (p->seq >= (1u << 28)) p->seq = 0;  // epochs stay distinct from the zero-initialised words
   const DecodeArgs d = decode_args(p, indices, offsets, psw, N, B, mean);
@@ -374,8 +381,8 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   p->max_D = max_D;
   p->uniform_D = uniform;
   const int nvec = max_D / 4;
-  for (int opt = 0; opt < 2; ++opt) {
-    emb_plan::RowSplit& sp = p->split[opt];
+  for (int si = 0; si < 3; ++si) {
+    emb_plan::RowSplit& sp = p->split[si];
     // 16-byte vectors each lane holds of a row (rows wider than kv*32 vectors are
     // cut into chunks). Narrow rows take more than they need, so that a row spans
     // only a few lanes and a warp works on several short runs at once (the short
@@ -383,12 +390,15 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     // loads in flight. Measured on GB300: rows of 9-32 vectors run fastest at
     // kv = 4 (the large skewed workload's reduce: 8.6 ms at kv = 1, 7.4 at 2, 6.1
     // at 4; the DLRM-like one 30.9 us at 2, 29.2 at 4); kv = 8 costs too much
-    // occupancy, so rows of 33-64 vectors stay at kv = 2, and SGD cuts rows wider
-    // than 64 vectors into chunks of 128 (kv = 4; the LM workload's 1024-vector
-    // rows: reduce 114.7 us in chunks of 64, 110.6 in chunks of 128). Row-wise
-    // Adagrad needs the whole row in one warp for its norm, so it widens kv instead.
+    // occupancy, so rows of 33-64 vectors stay at kv = 2. Wider rows: pooled
+    // per-element updates cut them into chunks of 128 vectors (kv = 4; pooled SGD,
+    // 4 x 200k rows, B = 4096, L = 20: D = 512 fp16 146.6 us per step at kv = 4,
+    // 160.9 at kv = 8), unpooled lookups into chunks of 256 (kv = 8; the LM
+    // workload's 1024-vector rows: reduce 114.7 us in chunks of 64, 110.6 in
+    // chunks of 128, 101.6 in chunks of 256). Row-wise Adagrad needs the whole row
+    // in one warp for its norm, so it widens kv instead.
     if (nvec <= 64) sp.kv = nvec <= 8 ? 1 : nvec <= 32 ? 4 : 2;
-    else sp.kv = opt == 0 ? 4 : nvec <= 128 ? 4 : 8;
+    else sp.kv = si == 0 ? 4 : (si == 2 || nvec > 128) ? 8 : 4;
     sp.C = (uint32_t)((nvec + sp.kv * 32 - 1) / (sp.kv * 32));
     auto shape = [&](int32_t t) {  // (chunks per row, lanes per lookup) of table t
       const int nv = (D_offsets[t + 1] - D_offsets[t]) / 4;
@@ -404,7 +414,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     sp.segs.push_back((uint32_t)T);
   }
   // the reduce counts (run x row chunk) tasks in 32 bits, with headroom
-  if ((uint64_t)std::max<int64_t>(max_N, 1) * std::max(p->split[0].C, p->split[1].C) >= (1ull << 31)) {
+  if ((uint64_t)std::max<int64_t>(max_N, 1) * std::max({p->split[0].C, p->split[1].C, p->split[2].C}) >= (1ull << 31)) {
     delete p;
     return EMB_ERR_INVALID_ARG;
   }
@@ -483,10 +493,10 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   // Each has a head and a tail partial row of kv*32 vectors.
   {
     const uint64_t warps = (uint64_t)max_grid * kWarps;
-    const uint64_t C = std::max(p->split[0].C, p->split[1].C);
+    const uint64_t C = std::max({p->split[0].C, p->split[1].C, p->split[2].C});
     p->cap_slices = (uint32_t)(warps + 5 * C + std::min<uint64_t>(64 * warps, C * (N / kMinSlice + 2)));
   }
-  const size_t part_row = (size_t)std::max(p->split[0].kv, p->split[1].kv) * 32 * sizeof(float4);
+  const size_t part_row = (size_t)std::max({p->split[0].kv, p->split[1].kv, p->split[2].kv}) * 32 * sizeof(float4);
   struct Seg {
     void** ptr;
     size_t bytes;
@@ -515,6 +525,8 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {reinterpret_cast<void**>(&p->split[1].d_segkeys), p->split[1].segs.size() * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->split[0].d_segs), p->split[0].segs.size() * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->split[1].d_segs), p->split[1].segs.size() * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[2].d_segkeys), p->split[2].segs.size() * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->split[2].d_segs), p->split[2].segs.size() * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->long_ids), p->cap_long * sizeof(uint32_t)},
       {reinterpret_cast<void**>(&p->longs), p->cap_long * sizeof(LongRun)},
       {reinterpret_cast<void**>(&p->partials), 2 * (size_t)p->cap_slices * part_row},
@@ -560,9 +572,9 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     for (int c = 0; c < 3; ++c)
       for (int wide = 0; wide < 2; ++wide)
         p->pass_cap[c][wide] = sort_pass_capacity(wide != 0, tiles[c], p->rbits, p->props.sms);
-    for (int opt = 0; opt < 2; ++opt)
+    for (int si = 0; si < 3; ++si)
       for (int it = 0; it < 2; ++it)
-        p->runs_cap[opt][it] = runs_capacity((int)p->split[opt].segs.size() - 1, it ? 16 : 8, p->props.sms);
+        p->runs_cap[si][it] = runs_capacity((int)p->split[si].segs.size() - 1, it ? 16 : 8, p->props.sms);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -120,7 +120,7 @@ def test_wide_rows_adagrad_unsupported():
         E.emb_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("D", [64, 4096])
+@pytest.mark.parametrize("D", [64, 260, 1028, 4096])
 @pytest.mark.parametrize("path", [E.EMB_NOBAG_SORTED, E.EMB_NOBAG_ATOMIC])
 def test_unpooled_multi_table(D, path):
     w = custom(7, [100, 3000, 17], [D, D, D], 3, lambda r, T, B: r.integers(0, 60, (T, B)),
