@@ -64,7 +64,7 @@ extern "C" {
 typedef enum {
   EMB_OK = 0,
   EMB_ERR_INVALID_ARG = 1,         /* bad argument, or malformed offsets found on the device */
-  EMB_ERR_UNSUPPORTED = 2,         /* valid but not supported by this build (see each call) */
+  EMB_ERR_UNSUPPORTED = 2,         /* valid but not supported by this library (see each call) */
   EMB_ERR_INDEX_OUT_OF_RANGE = 3,  /* an index outside [0, rows of its table) */
   EMB_ERR_OOM = 4,                 /* plan scratch could not be allocated */
   EMB_ERR_CUDA = 5,                /* a CUDA runtime call failed */
