@@ -49,7 +49,7 @@ DESCR = {
 TRAFFIC = {
     ("large", "reduce_update"): 8_444_050_688 + 2_477_037_568,
     ("dlrm", "reduce_update"): 21_105_152 + 1_792,
-    ("mixed", "reduce_update"): 679_966_464 + 186_059_520,
+    ("mixed", "reduce_update"): 686_998_784 + 196_492_800,
     ("lm", "reduce_update"): 399_763_200 + 85_659_648,
     ("lm", "atomic_scatter"): 418_241_536 + 115_250_432,
 }

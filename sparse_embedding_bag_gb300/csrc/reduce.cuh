@@ -87,15 +87,16 @@ struct PrefetchVals {
 
 // Minimum resident blocks per SM, by vectors per lane (register budget).
 // Measured on GB300: 2 vectors per lane run best at 3 blocks (80 registers)
-// with several team shapes (more loop state) or with the prefetch above, and at
-// 4 blocks (64 registers) otherwise. 8 vectors per lane run better at 2 blocks
+// with the prefetch above, and at 4 blocks (64 registers) otherwise, also with
+// several team shapes, where a few registers spill (the mixed-tables reduce
+// 538 us at 3 blocks, 517 at 4, 750 at 2). 8 vectors per lane run better at 2 blocks
 // (128 registers, a few spilled) than at 1 (223 registers) with one team shape:
 // the LM reduce 101.6 us; row-wise Adagrad on 4 x 200k rows, B = 4096, L = 20,
 // D = 1024 fp32 236.7 against 281.7 us per step, D = 768 fp16 234.6 against 302.2.
 template <int KV, bool MULTI, int VK>
 struct MinBlocks {
   static constexpr int value =
-      KV == 1 ? 4 : (KV == 2 ? ((MULTI || PrefetchVals<VK, MULTI>::value) ? 3 : 4) : (KV == 4 || !MULTI ? 2 : 1));
+      KV == 1 ? 4 : (KV == 2 ? (PrefetchVals<VK, MULTI>::value ? 3 : 4) : (KV == 4 || !MULTI ? 2 : 1));
 };
 
 // Sum over sorted positions [jb, je) of one run into acc by a team of lanes.
