@@ -173,11 +173,19 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
 
 // Lookups per thread of the large-batch tiles. Measured on GB300: 16 with two
 // resident blocks per SM (128 registers) beats 8 or 12 lookups per thread at
-// higher occupancy, and one block per SM with more registers.
+// higher occupancy, and one block per SM with more registers. With 32-bit
+// payloads three blocks per SM (80 registers, some spilled) do better still (the
+// large skewed workload's three passes 3.27 -> 3.19 ms); 64-bit payloads spill
+// more and stay at two (the mixed-tables passes 206 us, 223 at three).
 constexpr int kBigItems = 16;
 
+template <int ITEMS, typename V>
+struct PassBlocks {
+  static constexpr int value = ITEMS == kBigItems && sizeof(V) == 8 ? 2 : 3;
+};
+
 template <int ITEMS, typename V, int RADIX>
-__global__ void __launch_bounds__(kThreads, ITEMS == kBigItems ? 2 : 3) k_sort_pass(PassArgs a) {
+__global__ void __launch_bounds__(kThreads, PassBlocks<ITEMS, V>::value) k_sort_pass(PassArgs a) {
   constexpr int TILE = kThreads * ITEMS;
   constexpr int DPT = RADIX > kThreads ? RADIX / kThreads : 1;  // digits per thread
   extern __shared__ __align__(16) unsigned char smem[];
