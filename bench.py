@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="plain launches instead of programmatic dependent launches")
+    ap.add_argument("--front", default="auto", choices=["auto", "multiblock"],
+                    help="multiblock: sort every call with the multi-block front (A/B timing of the small-batch front)")
     ap.add_argument("--path", default="auto", choices=["auto", "sorted", "atomic"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--op", default="bwd", choices=["bwd", "fwd", "shard"],
@@ -724,7 +726,8 @@ def main():
     indices_h, offsets_h, grad_h, psw_h = host_arrays(w)
     step_bytes, reduce_bytes, uniq = algorithmic_bytes(w, variant)
     dw = dev.to_device(w, f"cuda:{local}")
-    flags = (E.EMB_FLAG_NO_PDL if args.no_pdl else 0) | (E.EMB_FLAG_STOCHASTIC_ROUNDING if variant == "sr" else 0)
+    flags = (E.EMB_FLAG_NO_PDL if args.no_pdl else 0) | (E.EMB_FLAG_STOCHASTIC_ROUNDING if variant == "sr" else 0) \
+        | (E.EMB_FLAG_NO_CLUSTER_FRONT if args.front == "multiblock" else 0)
     plan = dev.make_plan(w, device_index=local, flags=flags)
     path = {"auto": E.EMB_NOBAG_AUTO, "sorted": E.EMB_NOBAG_SORTED, "atomic": E.EMB_NOBAG_ATOMIC}[args.path]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=f"cuda:{local}")
@@ -897,7 +900,7 @@ def main():
                                "adagrad": "elementwise Adagrad",
                                "sr": "the workload's optimizer, stochastic rounding"}[variant],
                    "l2": "256 MB buffer written between timed steps", "cuda_graph": use_graph, "pdl": not args.no_pdl,
-                   "parallelism": f"{world} independent shard(s), no collective"},
+                   "front": args.front, "parallelism": f"{world} independent shard(s), no collective"},
         "hbm_gbs": step_bytes / (ms_job * 1e-3) / 1e9,
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,

@@ -96,6 +96,13 @@ typedef enum { EMB_NOBAG_AUTO = 0, EMB_NOBAG_SORTED = 1, EMB_NOBAG_ATOMIC = 2 } 
  * emb_plan_set_rounding sets seed and number.
  * A call captured in a CUDA graph keeps the number it was captured with. */
 #define EMB_FLAG_STOCHASTIC_ROUNDING 0x4u
+/* Sort with the multi-block front (histogram kernel, radix passes, run-length
+ * kernel) even where the small-batch front applies. That front takes calls of
+ * at most 2^18 lookups whose tables fit one cluster of CTAs each, all resident
+ * at once; a cluster sorts and run-length encodes one table's lookups in
+ * shared memory in a single launch. For A/B timing and tests: both fronts
+ * give identical results. */
+#define EMB_FLAG_NO_CLUSTER_FRONT 0x8u
 /* Test only: every block that would wait on another one gives up at once and
  * reports EMB_ERR_TIMEOUT, exercising the error path without a real stall. */
 #define EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u

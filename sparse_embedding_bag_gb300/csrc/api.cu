@@ -37,6 +37,16 @@ constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups a reduce w
 // lookups per warp): reduce 26.7 us with a floor of 64, 27.3 at 128, 36.0 at 256.
 constexpr uint32_t kStaticMinSlice = 64;
 constexpr int kStages = 5;
+// Largest batch the small-batch front takes (its CTAs hold their slices of a
+// table in shared memory: ceil(N / 16) lookups each). Below it, a cluster per
+// table sorts and run-length encodes in one launch; measured on GB300, the
+// DLRM-like step (172k lookups over 8 tables) and the LM one (32k lookups, one
+// table) run faster that way than through the multi-block front.
+constexpr int64_t kCfMaxN = (int64_t)1 << 18;
+// CTAs per cluster, in order of preference: the largest size of which one
+// cluster per table fits on the GPU at once. Measured on GB300 at one CTA per
+// SM (shared memory above half an SM): 7 clusters of 16 CTAs, 8 of 12, 15 of 8.
+constexpr int kCfSizes[4] = {16, 12, 8, 4};
 
 struct DeviceGuard {
   int prev = -1;
@@ -120,6 +130,11 @@ struct emb_plan {
   int pass_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};  // [pass tile class][wide values]
   int runs_cap[3][2] = {{0, 0}, {0, 0}, {0, 0}};
   int fwd_grid[3] = {0, 0, 0};  // forward kernel grid per output type (0: not set up yet)
+  // Small-batch front: clusters of each size in kCfSizes that can be resident
+  // at once, per value kind (0: that cluster size does not fit), for calls of
+  // at most cf_max_N lookups.
+  int cf_clusters[3][4] = {};  // [value kind][kCfSizes index]
+  int64_t cf_max_N = 0;
   cudaStream_t last_stream = nullptr;
   int last_kind = 0;  // 0 none / empty, 1 sorted, 2 atomic
   int64_t last_N = 0;
@@ -220,6 +235,48 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   const bool pdl = !(p->flags & EMB_FLAG_NO_PDL);
 
   EMB_TRY(record(p, 0, s));
+  // the small-batch front: one cluster per table, all resident at once
+  int cl = 0;
+  size_t cf_sm = 0;
+  const uint32_t* d_segs = p->split[si].d_segs;
+  const uint32_t S = (uint32_t)p->split[si].segs.size() - 1;
+  const int fin = (passes - 1) & 1;  // the buffers the last pass writes (both fronts)
+  if (N <= p->cf_max_N) {
+    for (int i = 0; i < 4 && !cl; ++i) {
+      if (p->T > p->cf_clusters[vk][i]) continue;
+      cf_sm = cfront_smem(vk, p->radix, mean != 0, (uint32_t)((N + kCfSizes[i] - 1) / kCfSizes[i]));
+      if (cf_sm <= (size_t)p->props.smem_optin) cl = kCfSizes[i];
+    }
+  }
+  if (cl) {
+    EMB_CUDA(cudaMemsetAsync(p->ctl, 0, sizeof(Ctl), s));  // control block only
+    CfrontArgs ca;
+    ca.d = d;
+    ca.ctl = p->ctl;
+    ca.sticky = p->sticky;
+    ca.lb = lb0;
+    ca.lb.epoch = epoch + 6;
+    ca.keys[0] = p->keys[0];
+    ca.keys[1] = p->keys[1];
+    ca.vals[0] = p->vals[0];
+    ca.vals[1] = p->vals[1];
+    ca.passes = passes;
+    ca.rbits = p->rbits;
+    ca.cap = (uint32_t)((N + cl - 1) / cl);
+    ca.run_key = p->run_key;
+    ca.run_start = p->run_start;
+    ca.thr = p->thr;
+    ca.long_ids = p->long_ids;
+    ca.longs = p->longs;
+    ca.cap_long = p->cap_long;
+    ca.segs = d_segs;
+    ca.S = S;
+    ca.seg_runs = p->seg_runs;
+    EMB_CUDA(launch_cfront(ca, vk, p->radix, cl, p->T, cf_sm, s, pdl));
+    EMB_TRY(record(p, 1, s));  // one kernel: the sort and run-length stages are empty
+    EMB_TRY(record(p, 2, s));
+    EMB_TRY(record(p, 3, s));
+  } else {
   EMB_CUDA(cudaMemsetAsync(p->ctl, 0, p->clear_bytes, s));  // control block and per-table histograms
   // the linearised pairs go to buffer 1, which the first pass reads
   HistArgs ha{d,           p->ctl,       p->sticky, passes, tile, p->keys[1], p->vals[1],
@@ -249,7 +306,6 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.ordered = (int)pgrid <= p->pass_cap[pass_tile_class(ptile)][wide ? 1 : 0];
     EMB_CUDA(launch_sort_pass(pa, wide, ptile, pgrid, s, pdl));
   }
-  const int fin = (passes - 1) & 1;
   EMB_TRY(record(p, 2, s));
   RunsArgs ra;
   ra.keys = p->keys[fin];
@@ -267,10 +323,11 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   ra.longs = p->longs;
   ra.cap_long = p->cap_long;
   ra.seg_keys = p->split[si].d_segkeys;
-  ra.S = (uint32_t)p->split[si].segs.size() - 1;
+  ra.S = S;
   ra.seg_runs = p->seg_runs;
   EMB_CUDA(launch_runs(ra, items, s, pdl));
   EMB_TRY(record(p, 3, s));  // run-length and long-run partition are one kernel (no event 4)
+  }
 
   ReduceArgs r;
   r.ctl = p->ctl;
@@ -278,8 +335,8 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
   r.run_key = p->run_key;
   r.run_start = p->run_start;
   r.seg_runs = p->seg_runs;
-  r.segs = p->split[si].d_segs;
-  r.S = (uint32_t)p->split[si].segs.size() - 1;
+  r.segs = d_segs;
+  r.S = S;
   r.longs = p->longs;
   r.partials = p->partials;
   r.done = p->done;
@@ -484,7 +541,7 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
     p->max_pass_tiles = (uint32_t)(tiles + (uint64_t)T + 1);
   }
   const uint64_t status_words =
-      std::max<uint64_t>((uint64_t)p->max_pass_tiles << p->rbits, (N + kRleTile - 1) / kRleTile * 4);
+      std::max<uint64_t>({(uint64_t)p->max_pass_tiles << p->rbits, (N + kRleTile - 1) / kRleTile * 4, 3 * (uint64_t)T});
   p->cap_long = (uint32_t)(N / p->thr + 1);
   // Slices (row chunk x slice) the reduce cuts the long runs into: at most
   // warps + C with one slice per warp; with more (slices of at least
@@ -567,6 +624,20 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
   }
   if (e == cudaSuccess) e = sort_configure(p->props);
   if (e == cudaSuccess) e = runs_configure();
+  if (e == cudaSuccess) e = cfront_configure(p->props.smem_optin);
+  if (e == cudaSuccess && !(flags & EMB_FLAG_NO_CLUSTER_FRONT)) {
+    p->cf_max_N = std::min<int64_t>(max_N, kCfMaxN);
+    for (int vk = 0; vk < 3; ++vk)
+      for (int i = 0; i < 4; ++i) {
+        // shared memory of the largest eligible call (mean pooling's bag lengths
+        // included where they fit; a call that needs more takes the other front)
+        const uint32_t cap = (uint32_t)((std::max<int64_t>(p->cf_max_N, 1) + kCfSizes[i] - 1) / kCfSizes[i]);
+        size_t sm = cfront_smem(vk, p->radix, true, cap);
+        if (sm > (size_t)p->props.smem_optin) sm = cfront_smem(vk, p->radix, false, cap);
+        if (sm <= (size_t)p->props.smem_optin)
+          p->cf_clusters[vk][i] = cfront_max_clusters(vk, p->radix, kCfSizes[i], sm);
+      }
+  }
   if (e == cudaSuccess) {
     const int tiles[3] = {kThreads * 4, kThreads * 8, kThreads * 16};
     for (int c = 0; c < 3; ++c)

@@ -2,6 +2,9 @@
 //
 // Pipeline of one sorted call (all stream-ordered, no host synchronisation):
 //   memset(ctl) -> k_hist -> k_sort_pass x passes -> k_runs -> k_reduce
+// or, for batches small enough that every CTA of a per-table cluster holds its
+// slice in shared memory (cfront.cu):
+//   memset(ctl) -> k_cfront -> k_reduce
 //   k_hist      linearises every lookup (hash_size_cumsum[t] + idx), checks it
 //               against its table, validates the CSR offsets and builds, per
 //               table, the digit histograms of all radix passes over the row
@@ -159,6 +162,28 @@ struct RunsArgs {
   const uint32_t* seg_keys;  // [S+1]: first linear index of each segment, then the total rows
   uint32_t S;
   uint32_t* seg_runs;        // [S+1]
+};
+
+// Small-batch front (cfront.cu): one cluster of CTAs per table sorts and
+// run-length encodes the table's segment; outputs as k_sort_pass + k_runs.
+struct CfrontArgs {
+  DecodeArgs d;
+  Ctl* ctl;
+  uint32_t* sticky;
+  LookbackCfg lb;            // per-table look-back: 3 status words per table
+  uint32_t* keys[2];         // pass p writes keys[p & 1] (the last pass: the sorted keys)
+  void* vals[2];
+  int passes, rbits;         // the digit of pass p is bits [p*rbits, (p+1)*rbits) of the row index
+  uint32_t cap;              // lookups of one CTA's slice that its shared memory holds
+  uint32_t* run_key;
+  uint32_t* run_start;       // [U+1]
+  uint32_t thr;
+  uint32_t* long_ids;
+  LongRun* longs;
+  uint32_t cap_long;
+  const uint32_t* segs;      // [S+1]: first table of each segment of tables with one team shape
+  uint32_t S;
+  uint32_t* seg_runs;        // [S+1] (written when S > 1)
 };
 
 struct ReduceArgs {
@@ -631,6 +656,15 @@ cudaError_t sort_configure(const DevProps& p);
 int runs_items_for(int64_t N);
 cudaError_t launch_runs(const RunsArgs& a, int items, cudaStream_t s, bool pdl);
 cudaError_t runs_configure();
+
+// cfront.cu: the small-batch front. Shared memory of one CTA holding `cap`
+// lookups; most clusters of cl CTAs resident at once (0 if none fit); launch of
+// `clusters` clusters (one table each at a time, tables in order).
+size_t cfront_smem(int vk, int radix, bool mean, uint32_t cap);
+cudaError_t cfront_configure(int smem_optin);
+int cfront_max_clusters(int vk, int radix, int cl, size_t smem);
+cudaError_t launch_cfront(const CfrontArgs& a, int vk, int radix, int cl, int clusters, size_t smem,
+                          cudaStream_t s, bool pdl);
 
 // forward.cu: forward pooled lookup kernel of (weight type, output type, kv), or nullptr.
 const void* fwd_kernel(int weight_dtype, int out_dtype, int kv);

@@ -24,6 +24,7 @@ EMB_NOBAG_AUTO, EMB_NOBAG_SORTED, EMB_NOBAG_ATOMIC = 0, 1, 2
 EMB_FLAG_CHECK_INDICES = 0x1
 EMB_FLAG_NO_PDL = 0x2
 EMB_FLAG_STOCHASTIC_ROUNDING = 0x4
+EMB_FLAG_NO_CLUSTER_FRONT = 0x8
 EMB_FLAG_DEBUG_FORCE_TIMEOUT = 0x100
 
 # Every symbol include/embbwd.h declares (checked by the tests against the header).

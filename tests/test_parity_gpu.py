@@ -258,30 +258,48 @@ def _expect_status(w, status, path=E.EMB_NOBAG_AUTO, flags=0):
         assert np.array_equal(dw.momentum.cpu().numpy(), m0)
 
 
+# both fronts of the sorted path: the small-batch one (a cluster per table) and the multi-block one
+FRONTS = [0, E.EMB_FLAG_NO_CLUSTER_FRONT]
+
+
 @pytest.mark.parametrize("bad", [-1, 100, 1 << 40])
 @pytest.mark.parametrize("path", [E.EMB_NOBAG_SORTED, E.EMB_NOBAG_ATOMIC, None])
-def test_index_out_of_range_leaves_weights(bad, path):
+@pytest.mark.parametrize("front", FRONTS)
+def test_index_out_of_range_leaves_weights(bad, path, front):
     w = custom(17, [100, 50], [16, 16], 64, lambda r, T, B: r.integers(1, 5, (T, B)),
                nobag=path is not None, optimizer=synth.SGD)
     w.indices[w.N // 2] = bad
-    _expect_status(w, E.EMB_ERR_INDEX_OUT_OF_RANGE, path=path or E.EMB_NOBAG_AUTO)
+    _expect_status(w, E.EMB_ERR_INDEX_OUT_OF_RANGE, path=path or E.EMB_NOBAG_AUTO, flags=front)
 
 
-def test_malformed_offsets_detected():
+@pytest.mark.parametrize("front", FRONTS)
+def test_malformed_offsets_detected(front):
     w = custom(18, [100, 50], [16, 16], 64, lambda r, T, B: r.integers(1, 5, (T, B)),
                optimizer=synth.ROWWISE_ADAGRAD)
     w.offsets = w.offsets.copy()
     w.offsets[10], w.offsets[11] = w.offsets[11], w.offsets[10] - 1  # decreasing
-    _expect_status(w, E.EMB_ERR_INVALID_ARG)
+    _expect_status(w, E.EMB_ERR_INVALID_ARG, flags=front)
 
 
-def test_forced_lookback_timeout_is_reported_not_hung():
+@pytest.mark.parametrize("front", FRONTS)
+def test_malformed_table_bounds_detected(front):
+    # the first table's lookups claimed to end past the batch: every segment is
+    # clamped into the batch, nothing is read or written out of bounds
+    w = custom(22, [100, 50], [16, 16], 64, lambda r, T, B: r.integers(1, 5, (T, B)),
+               optimizer=synth.ROWWISE_ADAGRAD)
+    w.offsets = w.offsets.copy()
+    w.offsets[w.B] = w.N + 1000
+    _expect_status(w, E.EMB_ERR_INVALID_ARG, flags=front)
+
+
+@pytest.mark.parametrize("front", FRONTS)
+def test_forced_lookback_timeout_is_reported_not_hung(front):
     # many sort tiles, so some block must wait on another; the test flag makes
     # every such wait give up at once
     w = custom(19, [5000], [16], 2000, lambda r, T, B: r.integers(1, 8, (T, B)),
                optimizer=synth.ROWWISE_ADAGRAD)
     assert w.N > 4 * 1024
-    _expect_status(w, E.EMB_ERR_TIMEOUT, flags=E.EMB_FLAG_DEBUG_FORCE_TIMEOUT)
+    _expect_status(w, E.EMB_ERR_TIMEOUT, flags=E.EMB_FLAG_DEBUG_FORCE_TIMEOUT | front)
 
 
 def test_call_argument_errors():
