@@ -299,7 +299,6 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     pa.vals_out = p->vals[out];
     pa.thist = p->thist;
     pa.tile_map = p->tile_map;
-    pa.hsc = p->d_hsc;
     pa.pass = pass;
     pa.passes = passes;
     pa.rbits = p->rbits;

@@ -99,9 +99,10 @@ struct DecodeArgs {
 };
 
 // A tile of a radix pass: sorted positions [i0, i1) of table t, whose segment's
-// first tile is `first`.
+// first tile is `first`; seg0 is the first position of the table's segment and
+// kbase = hash_size_cumsum[t] (kept here so a pass reads one entry, not three).
 struct PassTile {
-  uint32_t t, i0, i1, first;
+  uint32_t t, i0, i1, first, seg0, kbase;
 };
 
 struct HistArgs {
@@ -130,7 +131,6 @@ struct PassArgs {
   void* vals_out;
   const uint32_t* thist;      // [T][passes][radix]
   const PassTile* tile_map;   // [ctl->pass_tiles]
-  const uint32_t* hsc;        // [T+1]
   int pass;
   int passes;
   int rbits;                  // the digit of pass p is bits [p*rbits, (p+1)*rbits) of the row index
@@ -250,6 +250,12 @@ struct AtomicArgs {
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
   uint64_t v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 

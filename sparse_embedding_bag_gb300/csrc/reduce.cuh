@@ -452,7 +452,11 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
 
   pdl_wait();
   pdl_trigger();
-  if (*(volatile uint32_t*)&a.ctl->err) return;  // a check failed earlier in this call
+  // one round trip: the error word, the counts of the front, the table metadata
+  const uint32_t err = ld_relaxed_u32(&a.ctl->err);
+  const uint32_t NL = ld_relaxed_u32(&a.ctl->num_long);
+  const uint32_t Ltot = ld_relaxed_u32(&a.ctl->long_lookups);
+  const uint32_t U = ld_relaxed_u32(&a.ctl->num_runs);
   for (uint32_t i = threadIdx.x; i <= a.T; i += kThreads) {
     s_hsc[i] = a.hsc[i];
     s_Do[i] = a.D_offsets[i];
@@ -463,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
       s_segrun[i] = a.seg_runs[i];
     }
   }
+  if (err) return;  // a check failed earlier in this call (the same word for every thread)
   __syncthreads();
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t C = a.C;
@@ -483,8 +488,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
   // about 16 slices per warp (six tables' slabs, more than L2 holds) gave
   // 6.16 ms and 15.1 GB of DRAM traffic, about 32 gave 5.89 ms, about 64 gave
   // 5.93 ms and 10.0 GB.
-  const uint32_t NL = *(volatile uint32_t*)&a.ctl->num_long;
-  const uint32_t Ltot = *(volatile uint32_t*)&a.ctl->long_lookups;
   if (Ltot > 0) {
     const uint64_t per_warp = ((uint64_t)Ltot * C + W - 1) / W;
     const bool dynamic = per_warp > kStaticSlice;
@@ -554,7 +557,6 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
   // the rounds of all segments, in order, go round-robin to the warps. All warps
   // thus sweep the keys together (rows updated at the same time lie close in
   // memory), and narrow tables pack several runs per warp.
-  const uint32_t U = *(volatile uint32_t*)&a.ctl->num_runs;
   // One round of a team: run bounds [start, end) and key, table t (kAnyTable:
   // found from the key), chunk c.
   constexpr uint32_t kAnyTable = 0xffffffffu;

@@ -60,7 +60,7 @@ __device__ __forceinline__ void build_tile_map(const HistArgs& a, uint32_t* scra
   for (uint32_t t = t0; t < t1; ++t) {
     const uint32_t s0 = seg(t), s1 = seg(t + 1), n = ntiles(s0, s1);
     for (uint32_t k = 0; k < n && base + k < a.tile_cap; ++k)
-      a.tile_map[base + k] = PassTile{t, s0 + k * pt, min(s0 + (k + 1) * pt, s1), base};
+      a.tile_map[base + k] = PassTile{t, s0 + k * pt, min(s0 + (k + 1) * pt, s1), base, s0, d.hsc[t]};
     base += n;
   }
   // valid offsets never reach the cap; malformed ones (whose passes do nothing) are cut at it
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
 // large skewed workload's three passes 3.27 -> 3.19 ms); 64-bit payloads spill
 // more and stay at two (the mixed-tables passes 206 us, 223 at three).
 constexpr int kBigItems = 16;
+constexpr int kRankGrp = 4;  // items of a thread whose warp peer masks are found together
 
 template <int ITEMS, typename V>
 struct PassBlocks {
@@ -199,21 +200,23 @@ __global__ void __launch_bounds__(kThreads, PassBlocks<ITEMS, V>::value) k_sort_
   const int64_t N = a.N;
   pdl_wait();
   pdl_trigger();
-  // malformed offsets: the segments are not trustworthy, every block leaves (none waits)
-  if (*(volatile uint32_t*)&a.ctl->err & kErrOffsets) return;
-
   // Tiles in look-back order: the block index when every block of the grid can be
   // resident at once (no block waits on one that cannot start), else a counter.
   if (!a.ordered && threadIdx.x == 0) s_misc[0] = atomicAdd(&a.ctl->tile_ctr[a.pass], 1u);
   for (int i = threadIdx.x; i < kWarps * RADIX; i += kThreads) s_whist[i] = 0;
   __syncthreads();
-  const uint32_t tile = a.ordered ? blockIdx.x : s_misc[0];
-  if (tile >= *(volatile uint32_t*)&a.ctl->pass_tiles) return;  // the grid is an upper bound
+  const uint32_t tile = a.ordered ? blockIdx.x : s_misc[0];  // < the grid <= the tile map's entries
+  // one round trip: the error word, the number of tiles and this tile's entry
+  const uint32_t err = ld_relaxed_u32(&a.ctl->err);
+  const uint32_t ntiles = ld_relaxed_u32(&a.ctl->pass_tiles);
   const PassTile tm = a.tile_map[tile];
+  // malformed offsets: the segments are not trustworthy, every block leaves (none waits);
+  // the grid is an upper bound on the tiles
+  if ((err & kErrOffsets) || tile >= ntiles) return;
   const uint32_t t = tm.t;
   const int64_t i0 = tm.i0, i1 = min((int64_t)tm.i1, N);
-  const uint32_t seg0 = tm.first == tile ? tm.i0 : a.tile_map[tm.first].i0;  // first lookup of the table
-  const uint32_t kbase = a.hsc[t];
+  const uint32_t seg0 = tm.seg0;    // first lookup of the table
+  const uint32_t kbase = tm.kbase;  // hash_size_cumsum[t]
   const uint32_t shift = (uint32_t)(a.pass * a.rbits), dmask = (1u << a.rbits) - 1u;
   const uint32_t channels = dmask + 1u;
   // this table's count of each of the thread's digits (digits tid*DPT .. tid*DPT+DPT-1)
@@ -239,21 +242,31 @@ __global__ void __launch_bounds__(kThreads, PassBlocks<ITEMS, V>::value) k_sort_
   // Warp-level multisplit ranking: stable within the warp's slice of the tile.
   const uint32_t lt = lanemask_lt();
   uint32_t* wh = s_whist + warp * RADIX;
+  // kRankGrp items at a time: their peer masks are found before the counts are
+  // updated (the updates form one chain through the warp's histogram)
 #pragma unroll
-  for (int k = 0; k < ITEMS; ++k) {
-    const int64_t pos = wbase + k * 32 + lane;
-    const bool valid = pos < i1;
-    const uint32_t digit = valid ? (((keys[k] - kbase) >> shift) & dmask) : (uint32_t)RADIX;
-    const uint32_t peers = __match_any_sync(kFull, digit);
-    const int leader = __ffs(peers) - 1;
-    uint32_t pre = 0;
-    if (lane == leader && valid) {
-      pre = wh[digit];
-      wh[digit] = pre + __popc(peers);
+  for (int k0 = 0; k0 < ITEMS; k0 += kRankGrp) {
+    uint32_t dg[kRankGrp], pm[kRankGrp];
+#pragma unroll
+    for (int u = 0; u < kRankGrp; ++u) {
+      const int64_t pos = wbase + (k0 + u) * 32 + lane;
+      dg[u] = pos < i1 ? (((keys[k0 + u] - kbase) >> shift) & dmask) : (uint32_t)RADIX;
     }
-    pre = __shfl_sync(kFull, pre, leader);
-    ranks[k] = pre + __popc(peers & lt);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kRankGrp; ++u) pm[u] = __match_any_sync(kFull, dg[u]);
+#pragma unroll
+    for (int u = 0; u < kRankGrp; ++u) {
+      const bool valid = dg[u] < (uint32_t)RADIX;
+      const int leader = __ffs(pm[u]) - 1;
+      uint32_t pre = 0;
+      if (lane == leader && valid) {
+        pre = wh[dg[u]];
+        wh[dg[u]] = pre + __popc(pm[u]);
+      }
+      pre = __shfl_sync(kFull, pre, leader);
+      ranks[k0 + u] = pre + __popc(pm[u] & lt);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
