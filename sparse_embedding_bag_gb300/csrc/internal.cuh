@@ -354,7 +354,7 @@ __device__ __forceinline__ void block_excl_scan2(uint32_t v0, uint32_t v1, uint3
 // bounded: after spin_limit polls the tile raises kErrTimeout and carries on with
 // what it has (its successors never wait forever, and nothing is updated in that
 // call).
-template <int DPT>
+template <int DPT, int kWin>
 __device__ __forceinline__ void lookback_channels(const LookbackCfg& lb, uint32_t tile, uint32_t first,
                                                   uint32_t channels, const uint32_t (&c)[DPT],
                                                   const uint32_t (&agg)[DPT], uint32_t (&excl)[DPT], Ctl* ctl,
@@ -372,8 +372,8 @@ __device__ __forceinline__ void lookback_channels(const LookbackCfg& lb, uint32_
   if (tile == first) return;
   // Windowed walk: kWin predecessors are read per poll (independent loads in
   // flight), so a chain of tiles that published only aggregates is crossed kWin
-  // tiles per memory round trip.
-  constexpr int kWin = 16;
+  // tiles per memory round trip; every poll reads kWin words per channel, so
+  // wide windows cost L2 traffic (see the callers for the measured choice).
   bool failed = lb.force_timeout != 0;
   int64_t j[DPT];
   bool done[DPT];
@@ -433,9 +433,10 @@ __device__ __forceinline__ void lookback_channels(const LookbackCfg& lb, uint32_
 }
 
 // Warp-wide decoupled look-back for one channel: all 32 lanes of a warp call
-// it; lane k reads predecessor (j - k), so each round crosses up to 32 tiles
-// that have published only aggregates. Same publication protocol and bounded
-// waits as lookback_channel. Returns the exclusive prefix in every lane.
+// it; lane k < WIN reads predecessor (j - k), so each round crosses up to WIN
+// tiles that have published only aggregates. Same publication protocol and
+// bounded waits as lookback_channels. Returns the exclusive prefix in every lane.
+template <int WIN>
 __device__ __forceinline__ uint32_t lookback_warp(const LookbackCfg& lb, uint32_t tile,
                                                   uint32_t channels, uint32_t c, uint32_t agg,
                                                   Ctl* ctl, uint32_t* sticky) {
@@ -453,7 +454,9 @@ __device__ __forceinline__ uint32_t lookback_warp(const LookbackCfg& lb, uint32_
   uint32_t polls = 0;
   while (!failed) {
     const int64_t idx = j - (int64_t)lane;
-    const uint64_t w = idx >= 0 ? ld_relaxed_u64(lb.status + (size_t)idx * channels + c) : (tag | kFlagInc);
+    const uint64_t w = lane >= (uint32_t)WIN ? 0ull  // past the window: not ready, the walk stops there
+                       : idx >= 0 ? ld_relaxed_u64(lb.status + (size_t)idx * channels + c)
+                                  : (tag | kFlagInc);
     const bool ready = (uint32_t)(w >> 32) == lb.epoch && (w & (kFlagAgg | kFlagInc));
     const uint32_t nr = __ballot_sync(0xffffffffu, !ready);
     const uint32_t inc = __ballot_sync(0xffffffffu, ready && (w & kFlagInc));
@@ -467,7 +470,7 @@ __device__ __forceinline__ uint32_t lookback_warp(const LookbackCfg& lb, uint32_
     excl += v;
     if (found) break;
     j -= take;
-    if (take < 32) {
+    if (take < (uint32_t)WIN) {
       if (++polls > lb.spin_limit) failed = true;
       else if (polls > 8) __nanosleep(polls > 128 ? 256 : 32);
     }

@@ -53,6 +53,13 @@ __device__ __forceinline__ uint32_t run_end_search(const uint32_t* __restrict__ 
   return (uint32_t)lo;
 }
 
+// Predecessor tiles a look-back warp reads per poll and count. Every poll's
+// loads are L2 traffic shared with the other tiles in flight: measured on GB300,
+// the large skewed workload's run-length kernel takes 615 us reading 32, 561 at
+// 16, 547 at 8, 563 at 4 (and 1370 at 128); the mixed-tables and DLRM-like ones
+// do not change between 8 and 32.
+constexpr int kRunsLookback = 8;
+
 // Dynamic shared memory: run-head positions [TILE+1], first keys of segments [S+1].
 template <int ITEMS>
 size_t runs_smem(uint32_t S) {
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) k_runs(RunsArgs a) {
   block_excl_scan2(n_long, n_llook, s_scan, &e_long, &e_llook, &t_long, &t_llook);
   if (warp < 3) {  // one warp per count
     const uint32_t agg = warp == 0 ? n_heads : warp == 1 ? t_long : t_llook;
-    const uint32_t b = lookback_warp(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);
+    const uint32_t b = lookback_warp<kRunsLookback>(a.lb, tile, 3, warp, agg, a.ctl, a.sticky);
     if (lane == 0) s_base[warp] = b;
   }
   __syncthreads();

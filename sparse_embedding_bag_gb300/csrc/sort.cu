@@ -180,6 +180,17 @@ __global__ void __launch_bounds__(kThreads) k_hist(HistArgs a) {
 constexpr int kBigItems = 16;
 constexpr int kRankGrp = 4;  // items of a thread whose warp peer masks are found together
 
+// Predecessor tiles a pass's look-back reads per poll and channel. Every poll of
+// a tile reads window x buckets status words, and with hundreds of tiles of one
+// table in flight that traffic, not the walk's length, sets the pace. Measured on
+// GB300 (three passes of the large skewed workload; mixed tables; DLRM-like):
+// windows of 64, 32, 16, 8, 4, 2, 1 gave 6.00, 3.58, 3.08, 2.58, 2.61, 2.45,
+// 2.70 ms; 321, 230, 193, 190, 189, 191, 195 us; DLRM-like 20.0-20.4 us for 1-8.
+template <int ITEMS>
+struct LookbackWin {
+  static constexpr int value = ITEMS >= kBigItems ? 2 : 4;
+};
+
 template <int ITEMS, typename V>
 struct PassBlocks {
   static constexpr int value = ITEMS == kBigItems && sizeof(V) == 8 ? 2 : 3;
@@ -292,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, PassBlocks<ITEMS, V>::value) k_sort_
   uint32_t ec, eg, tc, tg;
   block_excl_scan2(cs, gs, s_misc + 16, &ec, &eg, &tc, &tg);
   uint32_t excl[DPT];
-  lookback_channels<DPT>(a.lb, tile, tm.first, channels, dch, cnt, excl, a.ctl, a.sticky);
+  lookback_channels<DPT, LookbackWin<ITEMS>::value>(a.lb, tile, tm.first, channels, dch, cnt, excl, a.ctl,
+                                                     a.sticky);
 #pragma unroll
   for (int q = 0; q < DPT; ++q) {
     const uint32_t dg = dch[q];
