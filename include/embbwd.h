@@ -98,7 +98,7 @@ typedef enum { EMB_NOBAG_AUTO = 0, EMB_NOBAG_SORTED = 1, EMB_NOBAG_ATOMIC = 2 } 
 #define EMB_FLAG_STOCHASTIC_ROUNDING 0x4u
 /* Sort with the multi-block front (histogram kernel, radix passes, run-length
  * kernel) even where the small-batch front applies. That front takes calls of
- * at most 2^18 lookups whose tables fit one cluster of CTAs each, all resident
+ * at most 2^16 lookups whose tables fit one cluster of CTAs each, all resident
  * at once; a cluster sorts and run-length encodes one table's lookups in
  * shared memory in a single launch. For A/B timing and tests: both fronts
  * give identical results. */

@@ -37,12 +37,13 @@ constexpr uint32_t kMinSlice = 8;          // fewest long-run lookups a reduce w
 // lookups per warp): reduce 26.7 us with a floor of 64, 27.3 at 128, 36.0 at 256.
 constexpr uint32_t kStaticMinSlice = 64;
 constexpr int kStages = 5;
-// Largest batch the small-batch front takes (its CTAs hold their slices of a
-// table in shared memory: ceil(N / 16) lookups each). Below it, a cluster per
-// table sorts and run-length encodes in one launch; measured on GB300, the
-// DLRM-like step (172k lookups over 8 tables) and the LM one (32k lookups, one
-// table) run faster that way than through the multi-block front.
-constexpr int64_t kCfMaxN = (int64_t)1 << 18;
+// Largest batch the small-batch front takes. Its CTAs hold their slices of a
+// table in shared memory (ceil(N / CTAs per cluster) lookups each), which allows
+// up to about 2^18 lookups; measured on GB300 (CUDA graph, PDL, L2 flushed) it
+// runs the tiny batch in 24.5 instead of 29.1 us per step and the LM one (32k
+// lookups, one table) in 129.7 instead of 130.0 us, but the DLRM-like one (172k
+// lookups over 8 tables) in 61.3 instead of 61.0 us, so it stops at 2^16.
+constexpr int64_t kCfMaxN = (int64_t)1 << 16;
 // CTAs per cluster, in order of preference: the largest size of which one
 // cluster per table fits on the GPU at once. Measured on GB300 at one CTA per
 // SM (shared memory above half an SM): 7 clusters of 16 CTAs, 8 of 12, 15 of 8.

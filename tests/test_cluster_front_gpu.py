@@ -53,6 +53,8 @@ def run_front(w, flags, thr=0):
 
 
 def check_both_fronts(w, thr=0, expect_cluster=True):
+    """expect_cluster: True, the default plan takes the small-batch front; False,
+    the multi-block one; None, either."""
     wc, mc, rc, msc = run_front(w, 0, thr)
     wb, mb, rb, msb = run_front(w, E.EMB_FLAG_NO_CLUSTER_FRONT, thr)
     exp = oracle.runs(w.T, w.B, w.hash_size_cumsum, w.indices, w.offsets, thr or 32)
@@ -68,6 +70,8 @@ def check_both_fronts(w, thr=0, expect_cluster=True):
     # empty (back-to-back events, a few microseconds at most)
     if expect_cluster:
         assert msc[1] + msc[2] < 0.006, msc
+    elif expect_cluster is not None:  # the multi-block front: a radix-sort stage of its own
+        assert msc[1] > 0.006, msc
     assert msb[1] > 0.0, msb
     ew, em = oracle_step(w)
     compare_weights(w, wc, ew, exp["run_keys"])
@@ -76,7 +80,18 @@ def check_both_fronts(w, thr=0, expect_cluster=True):
 
 
 def test_dlrm_like():
-    check_both_fronts(synth.dlrm(3))
+    # the DLRM-like recipe (8 tables x 100k rows, D=64, Zipf(1.05), row-wise
+    # Adagrad) at a batch the small-batch front takes
+    w = custom(10, [100_000] * 8, [64] * 8, 512, lambda r, T, B: r.integers(1, 21, (T, B)),
+               optimizer=synth.ROWWISE_ADAGRAD)
+    assert 20_000 < w.N <= 1 << 16
+    check_both_fronts(w)
+
+
+def test_dlrm_full_batch_takes_the_multiblock_front():
+    w = synth.dlrm(3)
+    assert w.N > 1 << 16
+    check_both_fronts(w, expect_cluster=False)
 
 
 def test_lm_unpooled():
@@ -105,8 +120,8 @@ def test_one_table_holds_most_lookups():
         L = r.integers(0, 3, (T, B))
         L[1] = r.integers(40, 80, B)
         return L
-    w = custom(2, [400, 60000, 900], [16, 16, 16], 1500, lengths, optimizer=synth.ROWWISE_ADAGRAD)
-    assert w.N > 60000
+    w = custom(2, [400, 60000, 900], [16, 16, 16], 1000, lengths, optimizer=synth.ROWWISE_ADAGRAD)
+    assert 50000 < w.N <= 1 << 16
     check_both_fronts(w)
 
 
@@ -157,12 +172,12 @@ def test_many_tables():
     # more tables: clusters of 8 CTAs where 16 no longer fit at once, or the other front
     rows = [500 + 37 * t for t in range(14)]
     w = custom(8, rows, [16] * 14, 400, lambda r, T, B: r.integers(0, 10, (T, B)))
-    check_both_fronts(w, expect_cluster=False)
+    check_both_fronts(w, expect_cluster=None)
 
 
 def test_largest_small_batch():
-    # 2^18 lookups: the largest batch the small-batch front takes
-    B = 1 << 15
+    # 2^16 lookups: the largest batch the small-batch front takes
+    B = 1 << 13
     w = custom(9, [100_000, 100_000], [16, 16], B, lambda r, T, B: np.full((T, B), 4))
-    assert w.N == 1 << 18
+    assert w.N == 1 << 16
     check_both_fronts(w)
