@@ -47,11 +47,11 @@ DESCR = {
 # full size, in the metric's single pass; the others from full section captures);
 # a workload without an entry reports null.
 TRAFFIC = {
-    ("large", "reduce_update"): 8_444_050_688 + 2_477_037_568,
-    ("dlrm", "reduce_update"): 21_105_152 + 1_792,
-    ("mixed", "reduce_update"): 686_998_784 + 196_492_800,
-    ("lm", "reduce_update"): 399_763_200 + 85_659_648,
-    ("lm", "atomic_scatter"): 418_241_536 + 115_250_432,
+    ("large", "reduce_update"): 8_431_475_200 + 2_477_187_584,
+    ("dlrm", "reduce_update"): 21_103_360 + 1_792,
+    ("mixed", "reduce_update"): 686_832_384 + 196_421_632,
+    ("lm", "reduce_update"): 399_733_760 + 85_272_576,
+    ("lm", "atomic_scatter"): 418_342_144 + 114_398_976,
 }
 
 
