@@ -63,9 +63,13 @@ struct RowShape {
 };
 
 // Lookups gathered per lane group and step, unrolled for memory-level parallelism.
+// Measured on GB300: 4 vectors per lane take 3 lookups per step (the large skewed
+// workload's reduce 5.67 -> 5.56 ms against 2), 8 vectors per lane 2 (the LM
+// reduce 101.7 us, 108.0 at 3), 2 vectors per lane 4 (the mixed-tables reduce
+// 517 us, 531 at 2).
 template <int KV, typename grad_t>
 struct Unroll {
-  static constexpr int value = KV >= 4 ? 2 : 4;
+  static constexpr int value = KV == 4 ? 3 : (KV > 4 ? 2 : 4);
 };
 
 // Long-run lookups per warp up to which the reduce cuts one slice per warp and
