@@ -158,8 +158,10 @@ emb_status emb_bag_bwd_sgd(emb_plan* plan, void* weights, const int64_t* indices
                            emb_pooling mode, float lr, void* stream);
 
 /* Pooled backward + row-wise Adagrad, in place on `weights` and fp32 `momentum`.
- * Same arguments as emb_bag_bwd_sgd plus momentum and eps. Requires every D_t <= 1024
- * (one warp holds the whole row for the row-wise norm); otherwise EMB_ERR_UNSUPPORTED. */
+ * Same arguments as emb_bag_bwd_sgd plus momentum and eps. Rows of every supported
+ * width (D_t <= 4096): when some D_t > 1024 the reduce runs twice on the stream,
+ * first finding each row's new state from the sums of squares of its 1024-wide
+ * chunks (added in chunk order), then updating the weights. */
 emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* plan, void* weights, float* momentum,
                                        const int64_t* indices, const int64_t* offsets,
                                        int64_t N, int32_t B, const float* per_sample_weights,

@@ -121,6 +121,11 @@ struct emb_plan {
   LongRun* longs = nullptr;
   float4* partials = nullptr;
   uint32_t* done = nullptr;
+  // row-wise Adagrad of rows of several chunks (split[1].C > 1): per-run sums of
+  // squares of each chunk, arrival counters (zero between calls), new states
+  float* rw_ss = nullptr;
+  uint32_t* rw_cnt = nullptr;
+  float* rw_m = nullptr;
   uint32_t cap_long = 0, cap_slices = 0;
 
   uint32_t seq = 0;
@@ -366,9 +371,24 @@ emb_status run_sorted(emb_plan* p, int opt, int vk, void* weights, float* moment
     r.call_lo = (uint32_t)call;
     r.call_hi = (uint32_t)(call >> 32);
   }
+  r.rw_pass = 0;
+  r.rw_ss = p->rw_ss;
+  r.rw_cnt = p->rw_cnt;
+  r.rw_m = p->rw_m;
+  r.long_ids = p->long_ids;
   const void* fn = reduce_fn(p, opt, vk);
   if (!fn) return EMB_ERR_UNSUPPORTED;
   void* args[] = {&r};
+  if (opt == 1 && r.C > 1) {
+    // Row-wise Adagrad of rows of several chunks: the first launch finds every
+    // row's new state from its chunks' sums of squares, the second updates the
+    // weights; the reduce's work counters start again from zero in between.
+    r.rw_pass = 1;
+    EMB_CUDA(launch_kernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads),
+                           reduce_smem_bytes(p->T), s, args, pdl));
+    EMB_CUDA(cudaMemsetAsync(&p->ctl->slice_ctr[0][0], 0, sizeof(p->ctl->slice_ctr) + sizeof(p->ctl->round_ctr), s));
+    r.rw_pass = 2;
+  }
   EMB_CUDA(launch_kernel(fn, dim3(p->reduce_grid[opt][vk]), dim3(kThreads),
                          reduce_smem_bytes(p->T), s, args, pdl));
   EMB_TRY(record(p, 5, s));
@@ -588,6 +608,9 @@ emb_status emb_bwd_plan(emb_plan** out, int device, int32_t T, const int64_t* ha
       {reinterpret_cast<void**>(&p->longs), p->cap_long * sizeof(LongRun)},
       {reinterpret_cast<void**>(&p->partials), 2 * (size_t)p->cap_slices * part_row},
       {reinterpret_cast<void**>(&p->done), 4 * (size_t)p->cap_slices * sizeof(uint32_t)},
+      {reinterpret_cast<void**>(&p->rw_ss), p->split[1].C > 1 ? N * p->split[1].C * sizeof(float) : 0},
+      {reinterpret_cast<void**>(&p->rw_cnt), p->split[1].C > 1 ? N * sizeof(uint32_t) : 0},
+      {reinterpret_cast<void**>(&p->rw_m), p->split[1].C > 1 ? N * sizeof(float) : 0},
   };
   size_t total = 0;
   for (const Seg& sg : segs) total = align_up(total, 256) + sg.bytes;
@@ -697,7 +720,6 @@ emb_status emb_bag_bwd_rowwise_adagrad(emb_plan* p, void* weights, float* moment
   EMB_TRY(check_common(p, weights, indices, offsets, N, B, grad_output));
   if (mode != EMB_POOL_SUM && mode != EMB_POOL_MEAN) return EMB_ERR_INVALID_ARG;
   if (per_sample_weights && !aligned(per_sample_weights, 4)) return EMB_ERR_INVALID_ARG;
-  if (p->split[1].C != 1) return EMB_ERR_UNSUPPORTED;  // the row-wise norm needs the whole row in one warp
   if (N == 0) {
     p->last_kind = 0;
     return EMB_OK;

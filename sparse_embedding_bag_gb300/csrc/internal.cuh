@@ -214,6 +214,18 @@ struct ReduceArgs {
   uint32_t seed_lo, seed_hi, call_lo, call_hi;  // its random words: Philox key and call
   uint32_t thr, C;
   uint32_t min_slice;       // fewest long-run lookups per warp slice
+  // Row-wise Adagrad of rows wider than one chunk (C > 1) takes two launches of
+  // the reduce. rw_pass 1: every chunk of a run stores its sum of squares of G in
+  // rw_ss[run * C + chunk]; the last chunk of the run to arrive (rw_cnt, reset to
+  // 0 by it) adds them in chunk order, stores the new state to momentum and to
+  // rw_m[run]. rw_pass 2: every chunk recomputes its G (the same summation order,
+  // so the same bits) and applies w -= lr * G / (sqrt(rw_m[run]) + eps).
+  // rw_pass 0: one launch (whole rows in one chunk).
+  int rw_pass;
+  float* rw_ss;             // [max_N * C]
+  uint32_t* rw_cnt;         // [max_N], zero between calls
+  float* rw_m;              // [max_N]
+  const uint32_t* long_ids; // run index of every long run
 };
 
 struct FwdArgs {

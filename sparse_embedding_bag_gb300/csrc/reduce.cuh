@@ -60,6 +60,7 @@ struct RowShape {
   uint32_t cvec;      // vectors in the chunk
   uint32_t lg;        // log2 of lanes per lookup
   int64_t goff;       // column offset of the table in a gradient row
+  uint32_t run;       // index of the row's run (set where the two-launch row-wise update needs it)
 };
 
 // Lookups gathered per lane group and step, unrolled for memory-level parallelism.
@@ -208,6 +209,8 @@ template <typename emb_t, int OPT, int KV>
 __device__ __forceinline__ void load_row(const ReduceArgs& a, const RowShape& rs, bool active,
                                          uint32_t g, uint32_t li, float4 (&w)[KV]) {
   if constexpr (OPT == 0) active = active && !a.dense;
+  // rows of several chunks (8 vectors per lane only): the first of two launches updates no weights
+  if constexpr (OPT == 1 && KV == 8) active = active && a.rw_pass != 1;
   const emb_t* row = static_cast<const emb_t*>(a.weights) +
                      (active ? __ldg(&a.weights_offsets[rs.t]) + rs.idx * rs.D : 0);
 #pragma unroll
@@ -257,9 +260,35 @@ __device__ __forceinline__ void update_row(const ReduceArgs& a, const RowShape& 
       }
     }
     for (uint32_t off = 1; off < Lt; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float m_new = m_old + __fdiv_rn(ss, (float)rs.D);
-    mult = __fdiv_rn(a.lr, __fsqrt_rn(m_new) + a.eps);
-    if (active && tl == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
+    // Rows of several chunks take 8 vectors per lane (a row of more than 1024
+    // elements); the narrower kernels carry only the one-launch update.
+    const int rw_pass = KV == 8 ? a.rw_pass : 0;
+    if (rw_pass == 1) {  // rows of several chunks, first launch: the row's state only
+      if (active && tl == 0) {
+        const uint32_t crow = ((rs.D >> 2) + KV * 32 - 1) / (KV * 32);  // chunks of this row
+        float* slot = a.rw_ss + (size_t)rs.run * a.C;
+        slot[rs.cvec_off / (KV * 32)] = ss;
+        __threadfence();
+        if (atomicAdd(&a.rw_cnt[rs.run], 1u) == crow - 1) {  // the last chunk to arrive
+          __threadfence();
+          float tot = 0.f;
+          for (uint32_t k = 0; k < crow; ++k) tot += __ldcg(slot + k);
+          const float m_new = m_old + __fdiv_rn(tot, (float)rs.D);
+          a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
+          a.rw_m[rs.run] = m_new;
+          a.rw_cnt[rs.run] = 0;
+        }
+      }
+      return;
+    }
+    if (rw_pass == 2) {  // second launch: the state the first one stored
+      const float m_new = active ? a.rw_m[rs.run] : 0.f;
+      mult = __fdiv_rn(a.lr, __fsqrt_rn(m_new) + a.eps);
+    } else {
+      const float m_new = m_old + __fdiv_rn(ss, (float)rs.D);
+      mult = __fdiv_rn(a.lr, __fsqrt_rn(m_new) + a.eps);
+      if (active && tl == 0) a.momentum[__ldg(&a.momentum_offsets[rs.t]) + rs.idx] = m_new;
+    }
   }
   if (!active || g != 0) return;
   if constexpr (OPT == 0) {
@@ -528,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
         if (lr.lpos >= b0) break;
         RowShape rs;
         if (!make_shape<KV>(a, s_hsc, s_Do, lr.key, c, &rs)) continue;  // chunk past this row's end
+        if constexpr (OPT == 1 && KV == 8) rs.run = a.rw_pass ? __ldg(&a.long_ids[kl]) : 0u;
         const uint32_t p0 = lr.lpos, p1 = lr.lpos + lr.len;
         const bool whole = p0 >= a0 && p1 <= b0;
         const uint32_t Pg = 32u >> rs.lg;
@@ -565,16 +595,17 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
   // found from the key), chunk c.
   constexpr uint32_t kAnyTable = 0xffffffffu;
   auto round = [&](bool active, uint32_t start, uint32_t end, uint32_t key, uint32_t t, uint32_t c,
-                   uint32_t Lt, uint32_t tl) {
-    RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0};  // inactive teams: a harmless, in-range shape
+                   uint32_t Lt, uint32_t tl, uint32_t run) {
+    RowShape rs{0u, 0, 4u, 0u, 0u, 0u, 0, 0u};  // inactive teams: a harmless, in-range shape
     active = active && end - start < a.thr;
     if (active) {
       if (t == kAnyTable) t = a.T == 1 ? 0u : table_of(s_hsc, a.T, key);
       active = shape_in<KV>(s_hsc, s_Do, t, key, c, &rs);
+      rs.run = run;
     }
     if (!__any_sync(0xffffffffu, active)) return;
     if (!active) {
-      rs = RowShape{0u, 0, 4u, 0u, 0u, 0u, 0};
+      rs = RowShape{0u, 0, 4u, 0u, 0u, 0u, 0, 0u};
       start = end = 0;
     }
     const uint32_t Pt = Lt >> rs.lg;
@@ -628,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
       q = claim();
       meta(q, n_start, n_end, n_key);
       const uint32_t r = C == 1 ? task : task / C;
-      round(task < tasks, start, end, key, kAnyTable, task - r * C, Lt, tl);
+      round(task < tasks, start, end, key, kAnyTable, task - r * C, Lt, tl, r);
     }
   } else {
   uint32_t P = 0;  // rounds of the segments before
@@ -647,15 +678,15 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<KV, MULTI, VK>::value) k_r
     P += rounds;
     for (; q < rounds; q += W) {
       const uint32_t task = q * NT + team;
-      uint32_t start = 0, end = 0, key = 0, t = t0;
+      uint32_t start = 0, end = 0, key = 0, t = t0, r = 0;
       if (task < tasks) {
-        const uint32_t r = R0 + (Ct == 1 ? task : task / Ct);
+        r = R0 + (Ct == 1 ? task : task / Ct);
         start = a.run_start[r];
         end = a.run_start[r + 1];
         key = a.run_key[r];
         if (t1 - t0 > 1) t = t0 + table_of(s_hsc + t0, t1 - t0, key);
       }
-      round(task < tasks, start, end, key, t, Ct == 1 ? 0u : task % Ct, Lt, tl);
+      round(task < tasks, start, end, key, t, Ct == 1 ? 0u : task % Ct, Lt, tl, r);
     }
   }
   }

@@ -107,17 +107,50 @@ def test_wide_rows_sgd(D):
     run_and_check(w)
 
 
-def test_wide_rows_adagrad_unsupported():
-    w = custom(6, [40], [2048], 4, lambda r, T, B: r.integers(0, 5, (T, B)),
+@pytest.mark.parametrize("D", [1028, 2048, 4096])
+@pytest.mark.parametrize("wdt", [synth.F32, synth.F16])
+def test_wide_rows_rowwise_adagrad(D, wdt):
+    # rows of 2-4 chunks of 1024 (two launches: the state from the chunks' sums of
+    # squares, then the update) next to a narrow table of one chunk; hot rows whose
+    # runs are long, cut into slices
+    w = custom(6, [40, 300], [D, 64], 60, lambda r, T, B: r.integers(0, 80, (T, B)),
+               optimizer=synth.ROWWISE_ADAGRAD, weight_dtype=wdt, momentum_init=0.5)
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("pooling,weighted", [(synth.MEAN, True), (synth.SUM, True)])
+def test_wide_rows_rowwise_adagrad_scaled(pooling, weighted):
+    w = custom(23, [500, 70], [2048, 3072], 40, lambda r, T, B: r.integers(0, 30, (T, B)),
+               optimizer=synth.ROWWISE_ADAGRAD, pooling=pooling, weighted=weighted,
+               weight_dtype=synth.BF16, momentum_init=0.25)
+    run_and_check(w)
+
+
+def test_wide_rows_rowwise_adagrad_deterministic():
+    # two launches per call, repeated: bitwise the same results run to run, and a
+    # second call on the updated weights and state matches two oracle steps
+    w = custom(24, [64], [4096], 200, lambda r, T, B: r.integers(0, 40, (T, B)),
                optimizer=synth.ROWWISE_ADAGRAD)
-    dw = dev.to_device(w)
+    dw1, dw2 = dev.to_device(w), dev.to_device(w)
     plan = dev.make_plan(w)
     try:
-        with pytest.raises(E.EmbError) as e:
-            dev.step(plan, dw)
-        assert e.value.status == E.EMB_ERR_UNSUPPORTED
+        dev.step(plan, dw1)
+        dev.step(plan, dw2)
+        assert E.emb_plan_status(plan) == E.EMB_OK
+        assert np.array_equal(dev.weights_numpy(dw1).view(np.uint32), dev.weights_numpy(dw2).view(np.uint32))
+        assert np.array_equal(dw1.momentum.cpu().numpy().view(np.uint32), dw2.momentum.cpu().numpy().view(np.uint32))
+        dev.step(plan, dw1)
+        assert E.emb_plan_status(plan) == E.EMB_OK
     finally:
         E.emb_plan_destroy(plan)
+    ew, em = oracle_step(w)
+    w2 = custom(24, [64], [4096], 200, lambda r, T, B: r.integers(0, 40, (T, B)),
+                optimizer=synth.ROWWISE_ADAGRAD)
+    w2.weights, w2.momentum = ew, em
+    ew2, em2 = oracle_step(w2)
+    keys = oracle.runs(w.T, w.B, w.hash_size_cumsum, w.indices, w.offsets)["run_keys"]
+    compare_weights(w, dev.weights_numpy(dw1), ew2, keys)
+    np.testing.assert_allclose(dw1.momentum.cpu().numpy(), em2, rtol=1e-4, atol=1e-5)
 
 
 @pytest.mark.parametrize("D", [64, 260, 1028, 4096])
