@@ -47,10 +47,6 @@ DESCR = {
 # dominant kernel, from ncu captures of the current kernels (the large workload at
 # full size, in the metric's single pass; the others from full section captures);
 # a workload without an entry reports null.
-# Copy streams of the end-to-end measurement. Measured on GB300 (pinned host memory):
-# about 190-210 GB/s host to device with one stream or four, and on small batches the
-# extra copies and events of four streams cost more host time than the step.
-E2E_COPY_STREAMS = 1
 TRAFFIC = {
     ("large", "reduce_update"): 8_431_475_200 + 2_477_187_584,
     ("dlrm", "reduce_update"): 21_103_360 + 1_792,
@@ -740,20 +736,20 @@ def main():
     ew_state = torch.zeros(dw.weights.numel(), dtype=torch.float32, device=f"cuda:{local}") \
         if variant == "adagrad" else None
 
-    def call(d=None):
+    def call(d=None, stream=None):  # stream None: torch's current stream
         d = dw if d is None else d
         if variant == "dense":
             if w.nobag:
                 E.emb_nobag_bwd_dense_grad(plan, dense_buf, d.indices, d.offsets, w.N, w.B,
-                                           d.grad_output)
+                                           d.grad_output, stream)
             else:
                 E.emb_bag_bwd_dense_grad(plan, dense_buf, d.indices, d.offsets, w.N, w.B,
-                                         d.per_sample_weights, d.grad_output, w.pooling)
+                                         d.per_sample_weights, d.grad_output, w.pooling, stream)
         elif variant == "adagrad":
             E.emb_bag_bwd_adagrad(plan, d.weights, ew_state, d.indices, d.offsets, w.N, w.B,
-                                  d.per_sample_weights, d.grad_output, w.pooling, w.lr, w.eps)
+                                  d.per_sample_weights, d.grad_output, w.pooling, w.lr, w.eps, stream)
         else:
-            dev.step(plan, d, path=path)
+            dev.step(plan, d, path=path, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         call()
@@ -862,11 +858,12 @@ def main():
     # ---- end to end through the public API with host buffers: every step copies its
     # inputs (indices, offsets, gradient, per-sample weights) from pinned host memory
     # and reads the 4-byte status word back. As a training loop prefetches its next
-    # batch, step k+1's inputs are copied into a second set of device buffers while
-    # step k computes, on E2E_COPY_STREAMS copy streams; a buffer set is
-    # refilled only after the step that read it has finished. The time of the whole
-    # run (every copy, call and status read) divided by its steps is the step time;
-    # nothing is written between steps to evict L2 (each step's inputs are new copies).
+    # batch, step k+1's inputs are copied on a copy stream into a second set of
+    # device buffers while step k computes; a buffer set is refilled only after the
+    # step that read it has finished. The time of the whole run (every copy, call and
+    # status read) divided by its steps is the step time; nothing is written between
+    # steps to evict L2 (each step's inputs are new copies). The library's calls run
+    # on torch's default stream (passed explicitly), the copies on a second stream.
     pin = lambda a: None if a is None else torch.from_numpy(
         np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
     h_idx, h_off, h_grad, h_psw = pin(indices_h), pin(offsets_h), pin(grad_h), pin(psw_h)
@@ -875,38 +872,31 @@ def main():
     bufs = [dw, dataclasses.replace(dw, indices=spare(dw.indices), offsets=spare(dw.offsets),
                                     grad_output=spare(dw.grad_output),
                                     per_sample_weights=spare(dw.per_sample_weights))]
-    cstreams = [torch.cuda.Stream(device=f"cuda:{local}") for _ in range(E2E_COPY_STREAMS)]
-    copied = [[torch.cuda.Event() for _ in cstreams] for _ in bufs]
+    copies = [[(b.indices, h_idx), (b.offsets, h_off), (b.grad_output, h_grad)] +
+              ([(b.per_sample_weights, h_psw)] if h_psw is not None else []) for b in bufs]
+    copy_stream = torch.cuda.Stream(device=f"cuda:{local}")
+    compute_stream = torch.cuda.default_stream(torch.device(f"cuda:{local}"))
+    copied = [torch.cuda.Event() for _ in bufs]
     used = [torch.cuda.Event() for _ in bufs]
-    compute_stream = torch.cuda.current_stream()
 
-    def issue_copies(k):
-        b = bufs[k % 2]
-        pairs = [(b.indices, h_idx), (b.offsets, h_off), (b.grad_output, h_grad)]
-        if h_psw is not None:
-            pairs.append((b.per_sample_weights, h_psw))
-        for i, cs in enumerate(cstreams):
-            cs.wait_event(used[k % 2])  # the step that last read this buffer set is done
-            with torch.cuda.stream(cs):
-                for dst, src in pairs:
-                    n = src.numel()
-                    lo, hi = n * i // len(cstreams), n * (i + 1) // len(cstreams)
-                    if hi > lo:
-                        dst.view(-1)[lo:hi].copy_(src.view(-1)[lo:hi], non_blocking=True)
-            copied[k % 2][i].record(cs)
+    def issue_copies(k):  # on the copy stream (the current torch stream of e2e_run)
+        copy_stream.wait_event(used[k % 2])  # the step that last read this buffer set is done
+        for dst, src in copies[k % 2]:
+            dst.copy_(src, non_blocking=True)
+        copied[k % 2].record(copy_stream)
 
     def e2e_run(steps):
-        issue_copies(0)
-        for k in range(steps):
-            if k + 1 < steps:
-                issue_copies(k + 1)
-            for ev in copied[k % 2]:
-                compute_stream.wait_event(ev)
-            call(bufs[k % 2])
-            used[k % 2].record(compute_stream)
-            st = E.emb_plan_status(plan)  # waits for step k and reads the 4-byte status word back
-            if st != E.EMB_OK:
-                raise SystemExit(f"device status {E.status_string(st)}")
+        with torch.cuda.stream(copy_stream):
+            issue_copies(0)
+            for k in range(steps):
+                if k + 1 < steps:
+                    issue_copies(k + 1)
+                compute_stream.wait_event(copied[k % 2])
+                call(bufs[k % 2], compute_stream)
+                used[k % 2].record(compute_stream)
+                st = E.emb_plan_status(plan)  # waits for step k and reads the 4-byte status word back
+                if st != E.EMB_OK:
+                    raise SystemExit(f"device status {E.status_string(st)}")
 
     e2e_steps = min(max(3, K // 2), 200)
     e2e_run(2)  # warm-up
@@ -952,8 +942,8 @@ def main():
         "stage_ms": {n: float(v) for n, v in zip(names, stage) if n != "-"},
         "e2e": {"value": e2e_val, "unit": "lookups/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": 4,
-                "overlap": f"step k+1's inputs copied on {E2E_COPY_STREAMS} stream(s) into a second buffer set "
-                           "while step k computes; status read back every step; no L2 flush between steps"},
+                "overlap": "step k+1's inputs copied on a copy stream into a second buffer set while step k "
+                           "computes; status read back every step; no L2 flush between steps"},
         "gpu_launches": kernels_per_step * K,
         "clocks": clocks.summary(),
     }
