@@ -8,9 +8,9 @@
 // outputs bit for bit: the stable sort of each table's segment on its row
 // index, the unique keys with their run starts, the number of runs, and the
 // ordered compaction of the long runs with the prefix sum of their lengths.
-// What changes is where the work waits. On a batch of a few hundred thousand
-// lookups the multi-block front is a chain of dependent global round trips:
-// four launches, each with its decoupled look-back. Here:
+// What changes is where the work waits. On a small batch the multi-block front
+// is a chain of dependent global round trips: four launches, each with its
+// decoupled look-back. Here:
 //   * the lookups of table t form one contiguous segment (the offsets are
 //     table-major), so the table needs nothing from other tables but the
 //     number of runs before it;
@@ -25,8 +25,9 @@
 //   * the run counts before the table come from a decoupled look-back over the
 //     tables (one status word per table and count, 32 tables per poll).
 // Shared memory holds ceil(N / CTAs per cluster) lookups per CTA, which bounds
-// the batches this front takes (the host checks it); each table is at most the
-// whole batch, so every slice fits.
+// the batches this front can take (the host checks it, and takes the front only
+// up to 2^16 lookups, where it measured faster); each table is at most the whole
+// batch, so every slice fits.
 #include <cooperative_groups.h>
 
 #include "decode.cuh"
