@@ -300,8 +300,10 @@ def test_sgd_single_lookup_closed_form(oracle_mod):
     assert w[4:].tolist() == [7.0] * 4  # untouched table
 
 
-@pytest.mark.parametrize("D", [4, 16, 64, 256])
+@pytest.mark.parametrize("D", [4, 16, 64, 256, 1028, 2048, 4096])
 def test_adagrad_from_zero_closed_form(oracle_mod, D):
+    # (1028-4096: rows the device updates in two launches, its state from the sums
+    # of squares of 1024-wide chunks)
     rng = np.random.default_rng(D)
     g = rng.standard_normal((1, D)).astype(np.float32)
     w = rng.uniform(-1, 1, D).astype(np.float32)
