@@ -99,6 +99,24 @@ def host_arrays(w):
     return conv(w.indices), conv(w.offsets), conv(w.grad_output), conv(w.per_sample_weights)
 
 
+# Largest batch the library sorts with its one-launch small-batch front (a cluster of
+# CTAs per table); above it, or with EMB_FLAG_NO_CLUSTER_FRONT, the multi-block front.
+SMALL_FRONT_MAX_N = 1 << 16
+
+
+def step_stages(atomic, small_front, passes, reduce_launches=1):
+    """Kernels of one step by profiled stage (the five stages of emb_plan_stage_ms),
+    the stages' names, and the kernels per step. small_front: the call took the
+    one-launch small-batch front (its sort and run-length stages are empty)."""
+    if atomic:
+        return [1, 0, 0, 0, 1], ["index_check", "-", "-", "-", "atomic_scatter"], 2
+    if small_front:
+        return ([1, 0, 0, 0, reduce_launches], ["cluster_front", "-", "-", "-", "reduce_update"],
+                1 + reduce_launches)
+    return ([1, passes, 1, 0, reduce_launches], ["linearise_hist", "radix_sort", "run_length", "-", "reduce_update"],
+            2 + passes + reduce_launches)
+
+
 def radix_passes(w):
     """Radix passes of the sort: the row index of the largest table in digits of at most 9 bits."""
     row_bits = max(int(np.ceil(np.log2(max(int(np.max(w.rows)), 2)))), 1)
@@ -828,12 +846,15 @@ def main():
     E.emb_plan_set_profiling(plan, False)
     stage = np.mean(np.array(stage_runs), axis=0)
     atomic = w.nobag and path == E.EMB_NOBAG_ATOMIC
-    names = ["linearise_hist", "radix_sort", "run_length", "-", "reduce_update"]
-    if atomic:
-        names = ["index_check", "-", "-", "-", "atomic_scatter"]
     passes = radix_passes(w)
+    # the small-batch front: one launch, so the sort and run-length stages record nothing
+    small_front = (not atomic and args.front == "auto" and n_local <= SMALL_FRONT_MAX_N
+                   and float(stage[1] + stage[2]) < 0.006)
+    # row-wise Adagrad on rows wider than 1024 elements launches the reduce twice
+    reduce_launches = 2 if (variant == "update" and not w.nobag and w.optimizer == synth.ROWWISE_ADAGRAD
+                            and int(np.max(w.dims)) > 1024) else 1
     # launches per stage: the dominant kernel is the one with the longest launch
-    launches = [1, 0 if atomic else passes, 0 if atomic else 1, 0, 1]
+    launches, names, kernels_per_step = step_stages(atomic, small_front, passes, reduce_launches)
     per_launch = [t / n if n else 0.0 for t, n in zip(stage, launches)]
     dom = int(np.argmax(per_launch))
     peak, peak_kind = peaks()
@@ -847,6 +868,7 @@ def main():
         "index_check": 8 * N,
         "atomic_scatter": reduce_bytes,
     }
+    stage_bytes["cluster_front"] = stage_bytes["linearise_hist"] + stage_bytes["radix_sort"] + stage_bytes["run_length"]
     dom_name = names[dom]
     achieved = stage_bytes.get(dom_name, 0) / launches[dom] / (per_launch[dom] * 1e-3) / 1e9
     # measured DRAM bytes of one launch of the dominant kernel (null without a capture
@@ -910,7 +932,6 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_val = n_job / float(t[0])
 
-    kernels_per_step = 2 if atomic else 3 + passes  # hist, passes, run-length, reduce
     result = {
         "metric": METRIC,
         "value": n_job / (ms_job * 1e-3),

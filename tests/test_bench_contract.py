@@ -34,3 +34,20 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_reference_arm_other_ranks_are_silent():
     assert _run({"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_launches_per_step_follow_the_front():
+    # the kernels a step launches, which the bench line reports as gpu_launches
+    sys.path.insert(0, ROOT)
+    import bench
+    # multi-block front: histogram, the passes, run-length, reduce
+    launches, names, per_step = bench.step_stages(False, False, 2)
+    assert per_step == 5 and sum(launches) == 5 and names[1] == "radix_sort"
+    # the small-batch front: one launch for the whole front, then the reduce
+    launches, names, per_step = bench.step_stages(False, True, 2)
+    assert per_step == 2 and launches == [1, 0, 0, 0, 1] and names[0] == "cluster_front"
+    # unpooled atomic scatter: the index check and the scatter
+    assert bench.step_stages(True, False, 3)[2] == 2
+    # row-wise Adagrad on rows of several 1024-wide chunks: the reduce twice
+    assert bench.step_stages(False, False, 3, reduce_launches=2)[2] == 7
+    assert bench.step_stages(False, True, 3, reduce_launches=2)[2] == 3
