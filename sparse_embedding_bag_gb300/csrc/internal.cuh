@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <type_traits>
@@ -66,6 +67,10 @@ struct Ctl {
   // Reduce: short-run rounds claimed dynamically, the same way.
   uint32_t round_ctr[kWarps][32];
 };
+// The reduce's work counters are cleared together between its two launches of a
+// row-wise update of wide rows: one range.
+static_assert(offsetof(Ctl, round_ctr) == offsetof(Ctl, slice_ctr) + sizeof(Ctl::slice_ctr),
+              "the reduce's work counters must be adjacent");
 
 // Sort-value kinds: what travels with each key through the radix passes.
 enum ValueKind {
