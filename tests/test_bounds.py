@@ -1,6 +1,7 @@
 """The derived error bound of tests/_bounds.py against fp32 evaluations of the
 same updates done here in numpy (several summation orders: in lookup order,
-reversed, shuffled, pairwise), including updates that cancel; and its size where
+reversed, shuffled, pairwise, and the row-wise sum of squares by chunks as rows
+wider than one chunk take it), including updates that cancel; and its size where
 nothing cancels (well below one 16-bit spacing of the operands, so the 16-bit bars
 stay at one ulp there)."""
 import numpy as np
@@ -63,7 +64,11 @@ def device_like_update(w, opt, K, order, rng, w_old, m_old):
     if opt == SGD:
         return np.array([fma32(-lr, G[d], wrow[d]) for d in range(D)])
     if opt == ROWWISE_ADAGRAD:
-        ss = fp32_sum([fma32(G[d], G[d], 0.0) for d in range(D)], order)
+        sq = [fma32(G[d], G[d], 0.0) for d in range(D)]
+        if order == "chunked":  # a row of several chunks: each chunk's sum, then the sums in chunk order
+            ss = fp32_sum([fp32_sum(sq[c:c + 4], "forward") for c in range(0, D, 4)], "forward")
+        else:
+            ss = fp32_sum(sq, order)
         m = f32(f32(m_old[K]) + f32(ss / f32(D)))
         mult = f32(lr / f32(f32(np.sqrt(m)) + eps))
         return np.array([fma32(-mult, G[d], wrow[d]) for d in range(D)])
@@ -108,7 +113,7 @@ def test_bound_covers_fp32_evaluations(opt, cancel):
     bounds = update_bounds(w, opt, keys, w.weights, m_old)
     worst = 0.0
     for K, (eps, x) in zip(keys, bounds):
-        for order in ("forward", "reversed", "shuffled", "pairwise"):
+        for order in ("forward", "reversed", "shuffled", "pairwise", "chunked"):
             got = device_like_update(w, opt, K, order, rng, w.weights, m_old).astype(np.float64)
             err = np.abs(got - x)
             assert np.all(err <= eps), (K, order, (err / eps).max())
