@@ -97,6 +97,14 @@ def test_header_declares_status_codes_used_by_binding():
         assert name in text
     assert "EMB_FLAG_DEBUG_FORCE_TIMEOUT 0x100u" in text
     assert E.EMB_FLAG_DEBUG_FORCE_TIMEOUT == 0x100
+    # every plan flag of the header, with the binding's value
+    import re
+    flags = dict(re.findall(r"#define (EMB_FLAG_\w+) (0x[0-9a-fA-F]+)u", text))
+    assert set(flags) == {"EMB_FLAG_CHECK_INDICES", "EMB_FLAG_NO_PDL", "EMB_FLAG_STOCHASTIC_ROUNDING",
+                          "EMB_FLAG_NO_CLUSTER_FRONT", "EMB_FLAG_DEBUG_FORCE_TIMEOUT"}
+    for name, value in flags.items():
+        assert getattr(E, name) == int(value, 16), name
+    assert len(set(flags.values())) == len(flags)  # distinct bits
 
 
 def _shard(lib, T=2, W=2, rb=((0, 5, 10), (0, 3, 7)), max_B=4, out=True, cyclic=False):
